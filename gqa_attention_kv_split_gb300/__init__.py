@@ -1,0 +1,183 @@
+"""Python binding of libgqa -- GB300 (sm_103a) grouped-query attention kernels.
+
+Thin ctypes marshalling over the C ABI declared in ``include/gqa.h``; the
+functions carry the C entry points' names.  PyTorch is used only for device
+memory and the current stream: every step of the computation runs in the
+library's CUDA kernels.  There is no fallback: if ``libgqa.so`` is missing or
+fails to load, every call raises.
+
+    gqa_decode(q, kv, seq_lens, *, out=None, q_scale=1.0)
+    nvfp4_paged_ctx_attn(q_fp8, k_fp4, k_sf, v_fp4, v_sf, block_table, qo_indptr, kv_lens,
+                         *, q_scale=1.0, out_scale=1.0, out=None)
+    gqa_debug_dequant_pages(fp4, sf, block_table, kv_lens, max_kv)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "GqaError", "lib", "gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages",
+    "gqa_check_device_errors", "gqa_release_workspace", "LIB_PATH", "build",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgqa.so")
+HQ, HKV, D, PAGE = 32, 8, 128, 64
+
+_STATUS = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_UNSUPPORTED", 3: "GQA_ERR_DEVICE_MISMATCH",
+           4: "GQA_ERR_CUDA", 5: "GQA_ERR_OOM", 6: "GQA_ERR_TIMEOUT"}
+
+
+class GqaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libgqa.so in-tree for sm_103a."""
+    from .build_lib import build as _build
+    return _build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgqa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libgqa.so is not built ({LIB_PATH}); call "
+                                   "gqa_attention_kv_split_gb300.build() first")
+            L = ctypes.CDLL(LIB_PATH)
+            c = ctypes
+            vp, i32p, i64, f32 = c.c_void_p, c.c_void_p, c.c_int64, c.c_float
+            L.gqa_last_error.restype = c.c_char_p
+            L.gqa_version.restype = c.c_int
+            L.gqa_decode.argtypes = [vp, vp, i32p, vp, i64, i64, f32, vp]
+            L.gqa_decode.restype = c.c_int
+            L.nvfp4_paged_ctx_attn.argtypes = [vp, f32, vp, vp, vp, vp, i32p, i32p, i32p, vp, f32,
+                                               i64, i64, i64, i64, vp]
+            L.nvfp4_paged_ctx_attn.restype = c.c_int
+            L.gqa_debug_dequant_pages.argtypes = [vp, vp, i32p, i32p, vp, i64, i64, i64, i64, vp]
+            L.gqa_debug_dequant_pages.restype = c.c_int
+            L.gqa_check_device_errors.argtypes = [c.c_int, c.POINTER(c.c_uint32)]
+            L.gqa_check_device_errors.restype = c.c_int
+            L.gqa_release_workspace.argtypes = []
+            L.gqa_release_workspace.restype = c.c_int
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise GqaError(status, lib().gqa_last_error().decode(errors="replace"))
+
+
+def _stream_for(t: torch.Tensor):
+    if t.is_cuda:
+        return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+    if torch.cuda.is_available():
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return ctypes.c_void_p(0)
+
+
+def _need(t: torch.Tensor, name: str, dtypes, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}; expected {tuple(shape)}")
+
+
+def _p(t: torch.Tensor):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+_E4M3 = (torch.uint8, torch.float8_e4m3fn)
+
+
+def gqa_decode(q: torch.Tensor, kv: torch.Tensor, seq_lens: torch.Tensor, *, out: torch.Tensor | None = None,
+               q_scale: float = 1.0) -> torch.Tensor:
+    """FP16 GQA decode of one token per sequence (see include/gqa.h).
+
+    q [B,32,128] f16, kv [B,2,8,cap,128] f16, seq_lens [B] int32, all on one
+    CUDA device (asynchronous on its current stream) or all on the host
+    (staged through the device, synchronous).
+    """
+    B = q.shape[0]
+    _need(q, "q", (torch.float16,), (B, HQ, D))
+    if kv.dim() != 5:
+        raise ValueError("kv must be [batch, 2, 8, capacity, 128]")
+    _need(kv, "kv", (torch.float16,), (B, 2, HKV, kv.shape[3], D))
+    _need(seq_lens, "sequence_lengths", (torch.int32,), (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.float16,), (B, HQ, D))
+    _check(lib().gqa_decode(_p(q), _p(kv), _p(seq_lens), _p(out), B, kv.shape[3], float(q_scale), _stream_for(q)))
+    return out
+
+
+def nvfp4_paged_ctx_attn(q_fp8, k_fp4, k_sf, v_fp4, v_sf, block_table, qo_indptr, kv_lens, *,
+                         q_scale: float = 1.0, out_scale: float = 1.0, out=None) -> torch.Tensor:
+    """Paged NVFP4 context attention, bottom-right causal (see include/gqa.h).
+
+    Returns out_fp8 [total_q,32,128] as uint8 E4M3 codes (or writes `out`).
+    """
+    T = q_fp8.shape[0]
+    _need(q_fp8, "q_fp8", _E4M3, (T, HQ, D))
+    P = k_fp4.shape[0]
+    _need(k_fp4, "k_fp4", (torch.uint8,), (P, HKV, PAGE, D // 2))
+    _need(v_fp4, "v_fp4", (torch.uint8,), (P, HKV, PAGE, D // 2))
+    _need(k_sf, "k_sf", _E4M3, (P, HKV, PAGE, D // 16))
+    _need(v_sf, "v_sf", _E4M3, (P, HKV, PAGE, D // 16))
+    B = kv_lens.shape[0]
+    _need(block_table, "block_table", (torch.int32,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_pages_per_seq]")
+    _need(qo_indptr, "qo_indptr", (torch.int32,), (B + 1,))
+    _need(kv_lens, "kv_lens", (torch.int32,), (B,))
+    if out is None:
+        out = torch.empty((T, HQ, D), dtype=torch.uint8, device=q_fp8.device)
+    _need(out, "out", _E4M3, (T, HQ, D))
+    _check(lib().nvfp4_paged_ctx_attn(
+        _p(q_fp8), float(q_scale), _p(k_fp4), _p(k_sf), _p(v_fp4), _p(v_sf), _p(block_table), _p(qo_indptr),
+        _p(kv_lens), _p(out), float(out_scale), B, T, P, block_table.shape[1], _stream_for(q_fp8)))
+    return out
+
+
+def gqa_debug_dequant_pages(fp4, sf, block_table, kv_lens, max_kv: int) -> torch.Tensor:
+    """E4M3 codes [B, max_kv, 8, 128] from the context kernel's dequant routine."""
+    P = fp4.shape[0]
+    _need(fp4, "fp4", (torch.uint8,), (P, HKV, PAGE, D // 2))
+    _need(sf, "sf", _E4M3, (P, HKV, PAGE, D // 16))
+    B = kv_lens.shape[0]
+    _need(block_table, "block_table", (torch.int32,))
+    _need(kv_lens, "kv_lens", (torch.int32,), (B,))
+    out = torch.empty((B, max_kv, HKV, D), dtype=torch.uint8, device=fp4.device)
+    _check(lib().gqa_debug_dequant_pages(_p(fp4), _p(sf), _p(block_table), _p(kv_lens), _p(out), B, P,
+                                         block_table.shape[1], int(max_kv), _stream_for(fp4)))
+    return out
+
+
+def gqa_check_device_errors(device: int = 0) -> int:
+    """Synchronise `device`; return (and clear) the kernels' error word."""
+    w = ctypes.c_uint32(0)
+    st = lib().gqa_check_device_errors(int(device), ctypes.byref(w))
+    if st not in (0, 6, 1):
+        _check(st)
+    return int(w.value)
+
+
+def gqa_release_workspace() -> None:
+    _check(lib().gqa_release_workspace())

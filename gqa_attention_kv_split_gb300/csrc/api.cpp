@@ -1,0 +1,399 @@
+// api.cpp -- the C ABI of libgqa (include/gqa.h): argument validation,
+// device scoping, workspace ownership, host-buffer staging and launch.
+//
+// Launcher conventions follow "FlashInfer NVFP4 QKV GEMM 최적화: SM103a
+// Epilogue 통합 및 CUDA 런처 개선", section 2: every tensor must sit on one
+// device (checked per pointer), the call switches to that device and
+// restores the caller's (no current-device check), and a launch grid must be
+// positive.  Nothing here computes attention; every step of the path runs in
+// the kernels of decode.cu and ctx_nvfp4.cu.
+#include "../../include/gqa.h"
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string t_last_error;
+
+gqa_status fail(gqa_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+gqa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(GQA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+#define GQA_CUDA_TRY(expr, what)                   \
+  do {                                             \
+    cudaError_t _e = (expr);                       \
+    if (_e != cudaSuccess) return cuda_fail(_e, what); \
+  } while (0)
+
+// Switches to `dev` for the lifetime of the object; restores the previous
+// current device afterwards.
+class ScopedDevice {
+ public:
+  explicit ScopedDevice(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+    if (prev_ != dev) ok_ = (cudaSetDevice(dev) == cudaSuccess);
+    switched_ = (prev_ != dev) && ok_;
+  }
+  ~ScopedDevice() {
+    if (switched_ && prev_ >= 0) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = -1;
+  bool ok_ = true;
+  bool switched_ = false;
+};
+
+// Where a pointer lives.
+struct Where {
+  bool host;
+  int device;
+};
+
+gqa_status classify(const void* p, const char* name, Where* w) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "cudaPointerGetAttributes");
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    w->host = false;
+    w->device = a.device;
+  } else {
+    w->host = true;
+    w->device = -1;
+  }
+  (void)name;
+  return GQA_OK;
+}
+
+struct Arg {
+  const void* p;
+  const char* name;
+  size_t align;
+};
+
+// All pointers on one side: either the same device or all host.
+gqa_status locate(const std::vector<Arg>& args, Where* out) {
+  for (const Arg& a : args)
+    if (a.p == nullptr) return fail(GQA_ERR_INVALID_ARG, "%s is a null pointer", a.name);
+  Where first{};
+  for (size_t i = 0; i < args.size(); ++i) {
+    Where w;
+    gqa_status st = classify(args[i].p, args[i].name, &w);
+    if (st != GQA_OK) return st;
+    if (i == 0) {
+      first = w;
+    } else if (w.host != first.host || w.device != first.device) {
+      return fail(GQA_ERR_DEVICE_MISMATCH, "%s is on %s %d but %s is on %s %d", args[i].name,
+                  w.host ? "host" : "device", w.device, args[0].name, first.host ? "host" : "device",
+                  first.device);
+    }
+    if (!w.host && (reinterpret_cast<uintptr_t>(args[i].p) % args[i].align) != 0)
+      return fail(GQA_ERR_INVALID_ARG, "%s is not %zu-byte aligned", args[i].name, args[i].align);
+  }
+  *out = first;
+  return GQA_OK;
+}
+
+// Grow-only device scratch per (device, stream).
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+gqa_status workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
+  *out = nullptr;
+  if (bytes == 0) return GQA_OK;
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  Workspace& w = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+  if (w.bytes < bytes) {
+    if (w.ptr) {
+      // Work queued on this stream may still use the old buffer.
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    size_t grow = bytes + bytes / 8;
+    cudaError_t e = cudaMalloc(&w.ptr, grow);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      w.ptr = nullptr;
+      e = cudaMalloc(&w.ptr, bytes);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        w.ptr = nullptr;
+        return fail(GQA_ERR_OOM, "workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+      }
+      grow = bytes;
+    }
+    w.bytes = grow;
+  }
+  *out = w.ptr;
+  return GQA_OK;
+}
+
+// Carves 256-byte aligned sub-buffers out of one allocation.
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    size_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* gqa_last_error(void) { return t_last_error.c_str(); }
+
+int gqa_version(void) { return 100; }
+
+gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
+                      int64_t capacity, float q_scale, gqa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (batch < 1 || batch > 65535) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 65535]", (long long)batch);
+  if (capacity < 1 || capacity > 2147483647LL)
+    return fail(GQA_ERR_UNSUPPORTED, "capacity %lld outside [1, 2^31-1]", (long long)capacity);
+  if (!std::isfinite(q_scale)) return fail(GQA_ERR_INVALID_ARG, "q_scale is not finite");
+  Where where;
+  gqa_status st = locate({{q, "q", 16}, {kv, "kv", 16}, {seq_lens, "seq_lens", 4}, {out, "out", 16}}, &where);
+  if (st != GQA_OK) return st;
+
+  const gqa::DecodePlan plan = gqa::plan_decode(batch, capacity);
+  if (plan.n_splits < 1) return fail(GQA_ERR_INVALID_ARG, "launch grid must be positive");
+  const size_t part_bytes = gqa::decode_workspace_bytes(batch, plan);
+
+  if (!where.host) {
+    ScopedDevice sd(where.device);
+    if (!sd.ok()) return fail(GQA_ERR_CUDA, "cannot switch to device %d", where.device);
+    void* ws = nullptr;
+    if ((st = workspace(where.device, stream, part_bytes, &ws)) != GQA_OK) return st;
+    GQA_CUDA_TRY(gqa::launch_decode(q, kv, seq_lens, out, batch, capacity, q_scale, plan, ws, stream),
+                 "decode launch");
+    return GQA_OK;
+  }
+
+  // Host buffers: stage the bytes the kernels read, run, copy the result back.
+  int dev = 0;
+  GQA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  const size_t q_bytes = (size_t)batch * 32 * 128 * 2;
+  const size_t slab = (size_t)capacity * 128 * 2;  // one (b, K|V, g) slab
+  const size_t kv_bytes = (size_t)batch * 2 * 8 * slab;
+  Carver c;
+  const size_t o_q = c.take(q_bytes), o_kv = c.take(kv_bytes), o_len = c.take((size_t)batch * 4),
+               o_out = c.take(q_bytes), o_part = c.take(part_bytes);
+  void* ws = nullptr;
+  if ((st = workspace(dev, stream, c.off, &ws)) != GQA_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  GQA_CUDA_TRY(cudaMemcpyAsync(base + o_q, q, q_bytes, cudaMemcpyHostToDevice, stream), "copy q");
+  GQA_CUDA_TRY(cudaMemcpyAsync(base + o_len, seq_lens, (size_t)batch * 4, cudaMemcpyHostToDevice, stream),
+               "copy seq_lens");
+  for (int64_t b = 0; b < batch; ++b) {
+    int64_t len = seq_lens[b];
+    len = len < 0 ? 0 : (len > capacity ? capacity : len);
+    if (len == 0) continue;
+    // 16 slabs (K and V of 8 heads), each with its first len tokens.
+    const uint8_t* src = static_cast<const uint8_t*>(kv) + (size_t)b * 16 * slab;
+    GQA_CUDA_TRY(cudaMemcpy2DAsync(base + o_kv + (size_t)b * 16 * slab, slab, src, slab, (size_t)len * 256, 16,
+                                   cudaMemcpyHostToDevice, stream),
+                 "copy kv");
+  }
+  GQA_CUDA_TRY(gqa::launch_decode(base + o_q, base + o_kv, reinterpret_cast<const int32_t*>(base + o_len),
+                                  base + o_out, batch, capacity, q_scale, plan,
+                                  part_bytes ? base + o_part : nullptr, stream),
+               "decode launch");
+  GQA_CUDA_TRY(cudaMemcpyAsync(out, base + o_out, q_bytes, cudaMemcpyDeviceToHost, stream), "copy out");
+  GQA_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+  return GQA_OK;
+}
+
+gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_fp4, const void* k_sf,
+                                const void* v_fp4, const void* v_sf, const int32_t* block_table,
+                                const int32_t* qo_indptr, const int32_t* kv_lens, void* out_fp8,
+                                float out_scale, int64_t batch, int64_t total_q, int64_t num_pages,
+                                int64_t max_pages_per_seq, gqa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (batch < 1 || batch > (1 << 20))
+    return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 2^20]", (long long)batch);
+  if (total_q < 0 || total_q > 2147483647LL) return fail(GQA_ERR_INVALID_ARG, "total_q %lld out of range", (long long)total_q);
+  if (num_pages < 1 || num_pages > 2147483647LL) return fail(GQA_ERR_INVALID_ARG, "num_pages %lld out of range", (long long)num_pages);
+  if (max_pages_per_seq < 1 || max_pages_per_seq > (2147483647LL / 64))
+    return fail(GQA_ERR_INVALID_ARG, "max_pages_per_seq %lld out of range", (long long)max_pages_per_seq);
+  if (!std::isfinite(q_scale)) return fail(GQA_ERR_INVALID_ARG, "q_scale is not finite");
+  if (!std::isfinite(out_scale) || !(out_scale > 0.f)) return fail(GQA_ERR_INVALID_ARG, "out_scale must be finite and > 0");
+  Where where;
+  gqa_status st = locate({{q_fp8, "q_fp8", 16},
+                          {k_fp4, "k_fp4", 16},
+                          {k_sf, "k_sf", 16},
+                          {v_fp4, "v_fp4", 16},
+                          {v_sf, "v_sf", 16},
+                          {block_table, "block_table", 4},
+                          {qo_indptr, "qo_indptr", 4},
+                          {kv_lens, "kv_lens", 4},
+                          {out_fp8, "out_fp8", 16}},
+                         &where);
+  if (st != GQA_OK) return st;
+
+  gqa::CtxArgs a;
+  a.q_scale = q_scale;
+  a.out_scale = out_scale;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.num_pages = num_pages;
+  a.max_pages_per_seq = max_pages_per_seq;
+
+  if (!where.host) {
+    if (total_q == 0) return GQA_OK;
+    ScopedDevice sd(where.device);
+    if (!sd.ok()) return fail(GQA_ERR_CUDA, "cannot switch to device %d", where.device);
+    a.q = static_cast<const uint8_t*>(q_fp8);
+    a.k_fp4 = static_cast<const uint8_t*>(k_fp4);
+    a.k_sf = static_cast<const uint8_t*>(k_sf);
+    a.v_fp4 = static_cast<const uint8_t*>(v_fp4);
+    a.v_sf = static_cast<const uint8_t*>(v_sf);
+    a.block_table = block_table;
+    a.qo_indptr = qo_indptr;
+    a.kv_lens = kv_lens;
+    a.out = static_cast<uint8_t*>(out_fp8);
+    cudaError_t e = gqa::launch_ctx(a, stream);
+    if (e == cudaErrorNotSupported) return fail(GQA_ERR_UNSUPPORTED, "context kernel not available in this build");
+    GQA_CUDA_TRY(e, "ctx launch");
+    return GQA_OK;
+  }
+
+  // Host buffers: the host can read the metadata, so check it fully.
+  if (qo_indptr[0] != 0 || qo_indptr[batch] != total_q)
+    return fail(GQA_ERR_INVALID_ARG, "qo_indptr must start at 0 and end at total_q");
+  for (int64_t b = 0; b < batch; ++b) {
+    if (qo_indptr[b + 1] < qo_indptr[b]) return fail(GQA_ERR_INVALID_ARG, "qo_indptr decreases at %lld", (long long)b);
+    if (kv_lens[b] < 0 || (int64_t)kv_lens[b] > 64 * max_pages_per_seq)
+      return fail(GQA_ERR_INVALID_ARG, "kv_lens[%lld] = %d out of range", (long long)b, kv_lens[b]);
+    const int64_t np = ((int64_t)kv_lens[b] + 63) / 64;
+    for (int64_t p = 0; p < np; ++p) {
+      const int32_t pg = block_table[b * max_pages_per_seq + p];
+      if (pg < 0 || pg >= num_pages)
+        return fail(GQA_ERR_INVALID_ARG, "block_table[%lld][%lld] = %d outside [0, num_pages)", (long long)b,
+                    (long long)p, pg);
+    }
+  }
+  if (total_q == 0) return GQA_OK;
+  int dev = 0;
+  GQA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  const size_t q_bytes = (size_t)total_q * 32 * 128;
+  const size_t fp4_bytes = (size_t)num_pages * 8 * 64 * 64;
+  const size_t sf_bytes = (size_t)num_pages * 8 * 64 * 8;
+  const size_t bt_bytes = (size_t)batch * max_pages_per_seq * 4;
+  Carver c;
+  const size_t o_q = c.take(q_bytes), o_kf = c.take(fp4_bytes), o_ks = c.take(sf_bytes), o_vf = c.take(fp4_bytes),
+               o_vs = c.take(sf_bytes), o_bt = c.take(bt_bytes), o_qi = c.take((size_t)(batch + 1) * 4),
+               o_kl = c.take((size_t)batch * 4), o_out = c.take(q_bytes);
+  void* ws = nullptr;
+  if ((st = workspace(dev, stream, c.off, &ws)) != GQA_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const std::pair<size_t, std::pair<const void*, size_t>> copies[] = {
+      {o_q, {q_fp8, q_bytes}},  {o_kf, {k_fp4, fp4_bytes}}, {o_ks, {k_sf, sf_bytes}},
+      {o_vf, {v_fp4, fp4_bytes}}, {o_vs, {v_sf, sf_bytes}},   {o_bt, {block_table, bt_bytes}},
+      {o_qi, {qo_indptr, (size_t)(batch + 1) * 4}}, {o_kl, {kv_lens, (size_t)batch * 4}}};
+  for (const auto& cp : copies)
+    GQA_CUDA_TRY(cudaMemcpyAsync(base + cp.first, cp.second.first, cp.second.second, cudaMemcpyHostToDevice, stream),
+                 "stage input");
+  a.q = base + o_q;
+  a.k_fp4 = base + o_kf;
+  a.k_sf = base + o_ks;
+  a.v_fp4 = base + o_vf;
+  a.v_sf = base + o_vs;
+  a.block_table = reinterpret_cast<const int32_t*>(base + o_bt);
+  a.qo_indptr = reinterpret_cast<const int32_t*>(base + o_qi);
+  a.kv_lens = reinterpret_cast<const int32_t*>(base + o_kl);
+  a.out = base + o_out;
+  cudaError_t e = gqa::launch_ctx(a, stream);
+  if (e == cudaErrorNotSupported) return fail(GQA_ERR_UNSUPPORTED, "context kernel not available in this build");
+  GQA_CUDA_TRY(e, "ctx launch");
+  GQA_CUDA_TRY(cudaMemcpyAsync(out_fp8, base + o_out, q_bytes, cudaMemcpyDeviceToHost, stream), "copy out");
+  GQA_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+  return GQA_OK;
+}
+
+gqa_status gqa_debug_dequant_pages(const void* fp4, const void* sf, const int32_t* block_table,
+                                   const int32_t* kv_lens, void* out_e4m3, int64_t batch, int64_t num_pages,
+                                   int64_t max_pages_per_seq, int64_t max_kv, gqa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (batch < 1 || batch > 65535) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 65535]", (long long)batch);
+  if (num_pages < 1 || max_pages_per_seq < 1 || max_kv < 1 || max_kv > 64 * max_pages_per_seq)
+    return fail(GQA_ERR_INVALID_ARG, "bad num_pages / max_pages_per_seq / max_kv");
+  Where where;
+  gqa_status st = locate({{fp4, "fp4", 16}, {sf, "sf", 16}, {block_table, "block_table", 4},
+                          {kv_lens, "kv_lens", 4}, {out_e4m3, "out_e4m3", 16}},
+                         &where);
+  if (st != GQA_OK) return st;
+  if (where.host) return fail(GQA_ERR_UNSUPPORTED, "gqa_debug_dequant_pages takes device pointers only");
+  ScopedDevice sd(where.device);
+  if (!sd.ok()) return fail(GQA_ERR_CUDA, "cannot switch to device %d", where.device);
+  GQA_CUDA_TRY(gqa::launch_dequant_pages(static_cast<const uint8_t*>(fp4), static_cast<const uint8_t*>(sf),
+                                         block_table, kv_lens, static_cast<uint8_t*>(out_e4m3), batch, num_pages,
+                                         max_pages_per_seq, max_kv, stream),
+               "dequant launch");
+  return GQA_OK;
+}
+
+gqa_status gqa_check_device_errors(int device, uint32_t* word) {
+  if (!word) return fail(GQA_ERR_INVALID_ARG, "word is a null pointer");
+  *word = 0;
+  ScopedDevice sd(device);
+  if (!sd.ok()) return fail(GQA_ERR_CUDA, "cannot switch to device %d", device);
+  uint32_t a = 0, b = 0;
+  GQA_CUDA_TRY(gqa::decode_read_errors(&a), "read decode error word");
+  GQA_CUDA_TRY(gqa::ctx_read_errors(&b), "read ctx error word");
+  *word = a | b;
+  if (*word & 1u) return fail(GQA_ERR_TIMEOUT, "a kernel's bounded wait expired (error word 0x%x)", *word);
+  if (*word) return fail(GQA_ERR_INVALID_ARG, "a kernel skipped out-of-range indices (error word 0x%x)", *word);
+  return GQA_OK;
+}
+
+gqa_status gqa_release_workspace(void) {
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  int prev = -1;
+  cudaGetDevice(&prev);
+  for (auto& kv : g_ws) {
+    if (kv.second.ptr) {
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ptr);
+    }
+  }
+  g_ws.clear();
+  if (prev >= 0) cudaSetDevice(prev);
+  return GQA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,471 @@
+// decode.cu -- FP16 grouped-query single-token decode, split-KV, for sm_103a.
+//
+// Operation ("NVIDIA SM110 GPU를 위한 실험적인 FP16 GQA 디코드 커널 추가",
+// section 1, the sm110_gqa_decode docstring, and section 3, the SDPA
+// comparator with enable_gqa=True):
+//   for every batch b and query head h (KV head g = h / 4),
+//   out[b,h,:] = softmax_t( q[b,h,:] . K[b,g,t,:] * q_scale / sqrt(128) ) V[b,g,t,:]
+//   over t < sequence_lengths[b], with K = kv[b,0], V = kv[b,1].
+//
+// Design (GB300 first; the page's 256/384-thread SM110 kernels are prior art
+// only):
+//  * Split kernel, grid (splits, 8 KV heads, batch).  Each CTA streams one
+//    chunk of tokens of one (b, g) slab.  A producer warp moves 16-token K and
+//    V tiles (4 KB each, contiguous in HBM) into an 8-stage shared-memory ring
+//    with 1-D bulk copies (TMA), completion tracked by mbarriers; the copies
+//    carry an L2 evict-first hint because every K/V byte is read exactly once.
+//  * Four consumer warps take whole stages round robin.  Each lane owns 8
+//    head-dim elements of one token (16-byte shared loads), computes the 4
+//    query heads' partial dot products, and a 16-lane reduce-scatter with
+//    shuffles leaves each lane two complete logits.  Online softmax runs in
+//    the exp2 domain (log2 e folded into the query scale), P is broadcast
+//    through shared memory, and PV accumulates in fp32 registers.
+//  * The four warps merge in shared memory and write one partial
+//    (m, l, o[128]) per (b, h, split); a second tiny kernel merges the splits
+//    by log-sum-exp.  When one split covers the capacity, the split kernel
+//    normalises and writes fp16 directly and no merge is launched.
+#include <cuda_fp16.h>
+
+#include <atomic>
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gqa {
+namespace {
+
+constexpr int kStageTok = 16;                         // tokens per ring stage
+constexpr int kStages = 8;                            // ring depth
+constexpr int kComputeWarps = 4;                      // consumer warps
+constexpr int kThreads = (kComputeWarps + 1) * 32;    // + one producer warp
+constexpr int kRowBytes = kD * 2;                     // one token of one head: 256 B
+constexpr int kStageBytes = kStageTok * kRowBytes;    // 4 KB of K (and of V)
+constexpr int kChunkQuantum = kStageTok * kComputeWarps;  // 64 tokens
+
+__device__ uint32_t g_decode_err;
+
+struct DecodeSmem {
+  alignas(1024) uint8_t k[kStages][kStageBytes];
+  alignas(128) uint8_t v[kStages][kStageBytes];
+  alignas(16) float p[kComputeWarps][kStageTok][kGroup];  // softmax weights, per warp
+  alignas(16) float o[kComputeWarps][kGroup][kD];         // per-warp partial outputs
+  float m[kComputeWarps][kGroup];
+  float l[kComputeWarps][kGroup];
+  alignas(8) uint64_t full[kStages];
+  alignas(8) uint64_t empty[kStages];
+};
+
+__device__ __forceinline__ void h8_to_f8(const uint4& u, float f[8]) {
+  const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __half22float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_split_kernel(const __half* __restrict__ q, const __half* __restrict__ kv,
+                        const int32_t* __restrict__ seq_lens, float* __restrict__ part_o,
+                        float2* __restrict__ part_ml, __half* __restrict__ out, int64_t cap, int chunk,
+                        int n_splits, float scale_log2) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  const int s = blockIdx.x;
+  const int g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int64_t len = seq_lens[b];
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  const int64_t t0 = (int64_t)s * chunk;
+  const bool direct = (n_splits == 1);
+
+  if (t0 >= len) {
+    // Nothing to read.  In direct mode (single split) this is an empty
+    // sequence: its output rows are zero.  Otherwise the merge covers it.
+    if (direct && warp < kComputeWarps) {
+      __half* dst = out + ((int64_t)b * kHq + g * kGroup + warp) * kD;
+      reinterpret_cast<uint2*>(dst)[lane] = make_uint2(0u, 0u);
+    }
+    return;
+  }
+  const int n_tok = (int)((len < t0 + chunk ? len : t0 + chunk) - t0);
+  const int n_st = (n_tok + kStageTok - 1) / kStageTok;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&sm.full[i]), 1);
+      mbar_init(smem_u32(&sm.empty[i]), 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kComputeWarps) {
+    // ---------------- producer: bulk copies of K and V tiles --------------
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const __half* kbase = kv + (((int64_t)b * 2 + 0) * kHkv + g) * cap * kD + t0 * kD;
+      const __half* vbase = kv + (((int64_t)b * 2 + 1) * kHkv + g) * cap * kD + t0 * kD;
+      for (int i = 0; i < n_st; ++i) {
+        const int st = i % kStages;
+        if (i >= kStages && !mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1, &g_decode_err)) break;
+        const int nt = min(kStageTok, n_tok - i * kStageTok);
+        const uint32_t bytes = (uint32_t)nt * kRowBytes;
+        const uint32_t fb = smem_u32(&sm.full[st]);
+        mbar_arrive_expect_tx(fb, 2 * bytes);
+        bulk_g2s_hint(smem_u32(sm.k[st]), kbase + (int64_t)i * kStageTok * kD, bytes, fb, pol);
+        bulk_g2s_hint(smem_u32(sm.v[st]), vbase + (int64_t)i * kStageTok * kD, bytes, fb, pol);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers ------------------------------------------------
+  const int hw = lane >> 4;  // which token of a pair this half-warp reads
+  const int j = lane & 15;   // head-dim slice [8j, 8j+8)
+  const int jt = j >> 1;     // token-pair permutation used by the reduce-scatter
+  const int jh = (j & 1) << 1;  // head permutation used by the reduce-scatter
+
+  // Query slice, pre-scaled into the exp2 domain.  Position h holds head
+  // (h ^ jh) so that every reduce-scatter step keeps its low half.
+  float qf[kGroup][8];
+#pragma unroll
+  for (int h = 0; h < kGroup; ++h) {
+    const uint4 u = *reinterpret_cast<const uint4*>(q + ((int64_t)b * kHq + g * kGroup + (h ^ jh)) * kD + 8 * j);
+    h8_to_f8(u, qf[h]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qf[h][e] *= scale_log2;
+  }
+
+  float o[kGroup][8];
+#pragma unroll
+  for (int h = 0; h < kGroup; ++h)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+  float m[kGroup] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  float lsum0 = 0.f, lsum1 = 0.f;  // running sums for heads jh, jh+1 (this lane's share)
+
+  bool ok = true;
+  for (int i = warp; i < n_st; i += kComputeWarps) {
+    const int st = i % kStages;
+    if (!mbar_wait(smem_u32(&sm.full[st]), (i / kStages) & 1, &g_decode_err)) {
+      ok = false;
+      break;
+    }
+    const int nt = min(kStageTok, n_tok - i * kStageTok);
+    const uint8_t* ks = sm.k[st];
+    const uint8_t* vs = sm.v[st];
+
+    // ---- S = q K^T: 8 tokens x 4 heads of partial sums per lane.
+    float part[32];
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) {
+      const int tl = 2 * (ii ^ jt) + hw;
+      float kf[8];
+      h8_to_f8(*reinterpret_cast<const uint4*>(ks + tl * kRowBytes + 16 * j), kf);
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+        float acc = qf[h][0] * kf[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) acc = fmaf(qf[h][e], kf[e], acc);
+        part[ii * kGroup + h] = acc;
+      }
+    }
+    // Reduce-scatter over the 16 lanes of the half-warp: keep low half, send
+    // high half.  Afterwards part[0..1] = full logits of token
+    // 2*jt + hw for heads jh, jh+1.
+#pragma unroll
+    for (int k = 0; k < 16; ++k) part[k] += __shfl_xor_sync(0xffffffffu, part[k + 16], 8);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) part[k] += __shfl_xor_sync(0xffffffffu, part[k + 8], 4);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) part[k] += __shfl_xor_sync(0xffffffffu, part[k + 4], 2);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) part[k] += __shfl_xor_sync(0xffffffffu, part[k + 2], 1);
+
+    const int tok = 2 * jt + hw;
+    float s0 = tok < nt ? part[0] : -INFINITY;
+    float s1 = tok < nt ? part[1] : -INFINITY;
+
+    // ---- tile maxima per head: the 16 lanes sharing jh, then swap pairs.
+    float t0m = s0, t1m = s1;
+#pragma unroll
+    for (int mask = 2; mask <= 16; mask <<= 1) {
+      t0m = fmaxf(t0m, __shfl_xor_sync(0xffffffffu, t0m, mask));
+      t1m = fmaxf(t1m, __shfl_xor_sync(0xffffffffu, t1m, mask));
+    }
+    const float o0m = __shfl_xor_sync(0xffffffffu, t0m, 1);
+    const float o1m = __shfl_xor_sync(0xffffffffu, t1m, 1);
+    const bool lo_pair = (jh == 0);
+    float tmax[kGroup];
+    tmax[0] = lo_pair ? t0m : o0m;
+    tmax[1] = lo_pair ? t1m : o1m;
+    tmax[2] = lo_pair ? o0m : t0m;
+    tmax[3] = lo_pair ? o1m : t1m;
+
+    float mnew[kGroup], alpha[kGroup];
+    bool rescale = false;
+#pragma unroll
+    for (int h = 0; h < kGroup; ++h) {
+      mnew[h] = fmaxf(m[h], tmax[h]);
+      rescale |= (mnew[h] != m[h]);
+      alpha[h] = fast_exp2(m[h] - mnew[h]);
+    }
+    const float p0 = fast_exp2(s0 - (lo_pair ? mnew[0] : mnew[2]));
+    const float p1 = fast_exp2(s1 - (lo_pair ? mnew[1] : mnew[3]));
+    lsum0 = fmaf(lsum0, lo_pair ? alpha[0] : alpha[2], p0);
+    lsum1 = fmaf(lsum1, lo_pair ? alpha[1] : alpha[3], p1);
+    *reinterpret_cast<float2*>(&sm.p[warp][tok][jh]) = make_float2(p0, p1);
+    __syncwarp();
+
+    if (rescale) {
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[h][e] *= alpha[h];
+        m[h] = mnew[h];
+      }
+    }
+
+    // ---- O += P V over this lane's 8 tokens.
+    if (nt == kStageTok) {
+#pragma unroll
+      for (int ii = 0; ii < 8; ++ii) {
+        const int tl = 2 * ii + hw;
+        const float4 pp = *reinterpret_cast<const float4*>(&sm.p[warp][tl][0]);
+        float vf[8];
+        h8_to_f8(*reinterpret_cast<const uint4*>(vs + tl * kRowBytes + 16 * j), vf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          o[0][e] = fmaf(pp.x, vf[e], o[0][e]);
+          o[1][e] = fmaf(pp.y, vf[e], o[1][e]);
+          o[2][e] = fmaf(pp.z, vf[e], o[2][e]);
+          o[3][e] = fmaf(pp.w, vf[e], o[3][e]);
+        }
+      }
+    } else {
+      for (int ii = 0; ii < 8; ++ii) {
+        const int tl = 2 * ii + hw;
+        if (tl >= nt) continue;  // rows past the copied tokens hold stale data
+        const float4 pp = *reinterpret_cast<const float4*>(&sm.p[warp][tl][0]);
+        float vf[8];
+        h8_to_f8(*reinterpret_cast<const uint4*>(vs + tl * kRowBytes + 16 * j), vf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          o[0][e] = fmaf(pp.x, vf[e], o[0][e]);
+          o[1][e] = fmaf(pp.y, vf[e], o[1][e]);
+          o[2][e] = fmaf(pp.z, vf[e], o[2][e]);
+          o[3][e] = fmaf(pp.w, vf[e], o[3][e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
+  }
+
+  // ---- per-warp finalisation: full row sums, fold the two half-warps.
+#pragma unroll
+  for (int mask = 2; mask <= 16; mask <<= 1) {
+    lsum0 += __shfl_xor_sync(0xffffffffu, lsum0, mask);
+    lsum1 += __shfl_xor_sync(0xffffffffu, lsum1, mask);
+  }
+  const float l_o0 = __shfl_xor_sync(0xffffffffu, lsum0, 1);
+  const float l_o1 = __shfl_xor_sync(0xffffffffu, lsum1, 1);
+#pragma unroll
+  for (int h = 0; h < kGroup; ++h)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], 16);
+  if (hw == 0) {
+#pragma unroll
+    for (int h = 0; h < kGroup; ++h) {
+      *reinterpret_cast<float4*>(&sm.o[warp][h][8 * j]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+      *reinterpret_cast<float4*>(&sm.o[warp][h][8 * j + 4]) = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+    }
+  }
+  if (lane == 0) {  // lane 0 has jh = 0
+#pragma unroll
+    for (int h = 0; h < kGroup; ++h) sm.m[warp][h] = m[h];
+    sm.l[warp][0] = lsum0;
+    sm.l[warp][1] = lsum1;
+    sm.l[warp][2] = l_o0;
+    sm.l[warp][3] = l_o1;
+  }
+  named_bar_sync(1, kComputeWarps * 32);
+  if (!ok) return;
+
+  // ---- merge the four warps; warp w finishes head w of the group.
+  const int h = warp;
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, sm.m[w][h]);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kComputeWarps; ++w) {
+    const float f = fast_exp2(sm.m[w][h] - M);  // 0 for a warp that saw no token
+    L = fmaf(sm.l[w][h], f, L);
+    const float4 ow = *reinterpret_cast<const float4*>(&sm.o[w][h][4 * lane]);
+    acc.x = fmaf(ow.x, f, acc.x);
+    acc.y = fmaf(ow.y, f, acc.y);
+    acc.z = fmaf(ow.z, f, acc.z);
+    acc.w = fmaf(ow.w, f, acc.w);
+  }
+  const int64_t row = (int64_t)b * kHq + g * kGroup + h;
+  if (direct) {
+    const float inv = 1.f / L;
+    __half2 lo = __floats2half2_rn(acc.x * inv, acc.y * inv);
+    __half2 hi = __floats2half2_rn(acc.z * inv, acc.w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(out + row * kD)[lane] = pk;
+  } else {
+    reinterpret_cast<float4*>(part_o + (row * n_splits + s) * kD)[lane] = acc;
+    if (lane == 0) part_ml[row * n_splits + s] = make_float2(M, L);
+  }
+}
+
+// Log-sum-exp merge of the per-split partials.  One CTA of 4 warps per
+// (b, h); warp w folds splits w, w+4, ...; lane owns 4 head-dim elements.
+__global__ void __launch_bounds__(128)
+    decode_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                        const int32_t* __restrict__ seq_lens, __half* __restrict__ out, int64_t cap, int chunk,
+                        int n_splits) {
+  __shared__ float4 so[4][32];
+  __shared__ float sm_m[4], sm_l[4];
+  const int h = blockIdx.x;
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int64_t len = seq_lens[b];
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  const int nv = (int)((len + chunk - 1) / chunk);  // splits holding data
+  const int64_t row = (int64_t)b * kHq + h;
+  if (nv == 0) {
+    if (warp == 0) reinterpret_cast<uint2*>(out + row * kD)[lane] = make_uint2(0u, 0u);
+    return;
+  }
+  const float2* ml = part_ml + row * n_splits;
+  float M = -INFINITY;
+  for (int s = warp; s < nv; s += 4) M = fmaxf(M, ml[s].x);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = warp; s < nv; s += 4) {
+    const float2 v = ml[s];
+    const float f = fast_exp2(v.x - M);
+    L = fmaf(v.y, f, L);
+    const float4 ov = reinterpret_cast<const float4*>(part_o + (row * n_splits + s) * kD)[lane];
+    acc.x = fmaf(ov.x, f, acc.x);
+    acc.y = fmaf(ov.y, f, acc.y);
+    acc.z = fmaf(ov.z, f, acc.z);
+    acc.w = fmaf(ov.w, f, acc.w);
+  }
+  so[warp][lane] = acc;
+  if (lane == 0) {
+    sm_m[warp] = M;
+    sm_l[warp] = L;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float MM = fmaxf(fmaxf(sm_m[0], sm_m[1]), fmaxf(sm_m[2], sm_m[3]));
+  float LL = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float f = fast_exp2(sm_m[w] - MM);  // 0 for a warp with no split
+    LL = fmaf(sm_l[w], f, LL);
+    a.x = fmaf(so[w][lane].x, f, a.x);
+    a.y = fmaf(so[w][lane].y, f, a.y);
+    a.z = fmaf(so[w][lane].z, f, a.z);
+    a.w = fmaf(so[w][lane].w, f, a.w);
+  }
+  const float inv = 1.f / LL;
+  __half2 lo = __floats2half2_rn(a.x * inv, a.y * inv);
+  __half2 hi = __floats2half2_rn(a.z * inv, a.w * inv);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(out + row * kD)[lane] = pk;
+}
+
+std::atomic<uint64_t> g_smem_ready{0};  // per-device bit: smem opt-in done
+
+cudaError_t ensure_smem_optin(int dev) {
+  const uint64_t bit = 1ull << (dev & 63);
+  if (g_smem_ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(DecodeSmem));
+  if (e != cudaSuccess) return e;
+  g_smem_ready.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int64_t batch, int64_t capacity) {
+  (void)batch;
+  DecodePlan p;
+  // A split is a whole number of 64-token quanta (4 warps x 16-token stages).
+  int chunk = 512;
+  if (const char* env = getenv("GQA_DECODE_SPLIT_TOKENS")) {
+    int v = atoi(env);
+    if (v >= kChunkQuantum) chunk = v;
+  }
+  chunk = (chunk + kChunkQuantum - 1) / kChunkQuantum * kChunkQuantum;
+  const int64_t cap_q = (capacity + kChunkQuantum - 1) / kChunkQuantum * kChunkQuantum;
+  if (cap_q <= chunk) chunk = (int)(cap_q > 0 ? cap_q : kChunkQuantum);
+  p.chunk = chunk;
+  p.n_splits = (int)((capacity + chunk - 1) / chunk);
+  if (p.n_splits < 1) p.n_splits = 1;
+  return p;
+}
+
+size_t decode_workspace_bytes(int64_t batch, const DecodePlan& plan) {
+  if (plan.n_splits <= 1) return 0;
+  const size_t rows = (size_t)batch * kHq * (size_t)plan.n_splits;
+  return rows * kD * sizeof(float) + rows * sizeof(float2);
+}
+
+cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
+                          int64_t capacity, float q_scale, const DecodePlan& plan, void* workspace,
+                          cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = ensure_smem_optin(dev)) != cudaSuccess) return e;
+  const float scale_log2 = q_scale / sqrtf((float)kD) * 1.4426950408889634f;
+  float* part_o = nullptr;
+  float2* part_ml = nullptr;
+  if (plan.n_splits > 1) {
+    const size_t rows = (size_t)batch * kHq * (size_t)plan.n_splits;
+    part_o = static_cast<float*>(workspace);
+    part_ml = reinterpret_cast<float2*>(part_o + rows * kD);
+  }
+  dim3 grid((unsigned)plan.n_splits, kHkv, (unsigned)batch);
+  decode_split_kernel<<<grid, kThreads, sizeof(DecodeSmem), stream>>>(
+      static_cast<const __half*>(q), static_cast<const __half*>(kv), seq_lens, part_o, part_ml,
+      static_cast<__half*>(out), capacity, plan.chunk, plan.n_splits, scale_log2);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (plan.n_splits > 1) {
+    dim3 mgrid(kHq, (unsigned)batch);
+    decode_merge_kernel<<<mgrid, 128, 0, stream>>>(part_o, part_ml, seq_lens, static_cast<__half*>(out),
+                                                   capacity, plan.chunk, plan.n_splits);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t decode_read_errors(uint32_t* word) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  uint32_t zero = 0;
+  if ((e = cudaMemcpyFromSymbol(word, g_decode_err, sizeof(uint32_t))) != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_decode_err, &zero, sizeof(uint32_t));
+}
+
+}  // namespace gqa

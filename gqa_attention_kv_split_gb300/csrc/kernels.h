@@ -1,0 +1,61 @@
+// kernels.h -- internal launch interface between the C-ABI layer (api.cpp)
+// and the CUDA translation units.  Not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gqa {
+
+// ---- FP16 split-KV decode -------------------------------------------------
+
+struct DecodePlan {
+  int chunk;     // tokens per split (multiple of 64)
+  int n_splits;  // splits per sequence = ceil(capacity / chunk)
+};
+
+// Split planning from the capacity and batch only (sequence lengths live on
+// the device and are never read by the host).
+DecodePlan plan_decode(int64_t batch, int64_t capacity);
+
+// Bytes of scratch the decode needs for its per-split partial results
+// (0 when a single split covers the capacity).
+size_t decode_workspace_bytes(int64_t batch, const DecodePlan& plan);
+
+cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
+                          int64_t capacity, float q_scale, const DecodePlan& plan, void* workspace,
+                          cudaStream_t stream);
+
+// Reads and clears the decode kernels' device error word on the current
+// device (synchronises the device).
+cudaError_t decode_read_errors(uint32_t* word);
+
+// ---- NVFP4 paged context attention --------------------------------------
+
+struct CtxArgs {
+  const uint8_t* q;            // [total_q, 32, 128] E4M3
+  const uint8_t* k_fp4;        // [num_pages, 8, 64, 64]
+  const uint8_t* k_sf;         // [num_pages, 8, 64, 8]
+  const uint8_t* v_fp4;
+  const uint8_t* v_sf;
+  const int32_t* block_table;  // [batch, max_pages_per_seq]
+  const int32_t* qo_indptr;    // [batch + 1]
+  const int32_t* kv_lens;      // [batch]
+  uint8_t* out;                // [total_q, 32, 128] E4M3
+  float q_scale;
+  float out_scale;
+  int64_t batch;
+  int64_t total_q;
+  int64_t num_pages;
+  int64_t max_pages_per_seq;
+};
+
+cudaError_t launch_ctx(const CtxArgs& a, cudaStream_t stream);
+
+cudaError_t launch_dequant_pages(const uint8_t* fp4, const uint8_t* sf, const int32_t* block_table,
+                                 const int32_t* kv_lens, uint8_t* out, int64_t batch, int64_t num_pages,
+                                 int64_t max_pages_per_seq, int64_t max_kv, cudaStream_t stream);
+
+cudaError_t ctx_read_errors(uint32_t* word);
+
+}  // namespace gqa

@@ -1,0 +1,168 @@
+/*
+ * gqa.h -- C ABI of libgqa: grouped-query attention kernels for NVIDIA GB300
+ * (sm_103a), head_dim 128, 32 query heads over 8 KV heads (4 query heads per
+ * KV head).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every tensor argument is a plain pointer to a dense, row-major
+ * (C-contiguous) array with the shape stated below.  All tensor pointers of
+ * one call must be either
+ *   - device memory of one and the same CUDA device (cudaMalloc'd, managed,
+ *     or a PyTorch CUDA tensor's data pointer): the call enqueues its kernels
+ *     on `stream` and returns without synchronising; or
+ *   - host memory (pageable or pinned): the call stages the inputs into a
+ *     library-owned device buffer on the calling thread's current device,
+ *     runs the same kernels on `stream`, copies the output back, and
+ *     synchronises `stream` before returning.
+ * Mixing host and device pointers, or device pointers of two devices, is
+ * rejected with GQA_ERR_DEVICE_MISMATCH.  Device pointers must be 16-byte
+ * aligned (GQA_ERR_INVALID_ARG otherwise).
+ *
+ * Device selection.  For device pointers the call switches to the pointers'
+ * device for its duration and restores the caller's current device on
+ * return; the caller's current device need not match.  (The launcher
+ * conventions of "FlashInfer NVFP4 QKV GEMM 최적화: SM103a Epilogue 통합 및 CUDA
+ * 런처 개선", section 2: all tensors on one device, scoped device switch, no
+ * current-device check, positive launch grid.)
+ *
+ * Ownership.  The caller owns every tensor.  The library owns a grow-only
+ * scratch workspace per (device, stream), released by
+ * gqa_release_workspace().  Two calls on the same stream are ordered by the
+ * stream; calls on different streams use different workspaces.
+ *
+ * Errors.  Every entry point returns a gqa_status; GQA_OK means the work was
+ * validated and enqueued (device pointers) or completed (host pointers).  On
+ * any other status nothing was launched, and gqa_last_error() returns a
+ * thread-local message.  No C++ exception crosses this boundary.
+ */
+#ifndef GQA_H_
+#define GQA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA runtime headers; 0 is the legacy
+ * default stream. */
+typedef struct CUstream_st* gqa_stream_t;
+
+typedef enum gqa_status {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = 1,      /* null pointer, bad size, misalignment */
+  GQA_ERR_UNSUPPORTED = 2,      /* shape outside what the kernels handle */
+  GQA_ERR_DEVICE_MISMATCH = 3,  /* pointers on different devices / host+device mix */
+  GQA_ERR_CUDA = 4,             /* a CUDA runtime call failed */
+  GQA_ERR_OOM = 5,              /* workspace allocation failed */
+  GQA_ERR_TIMEOUT = 6           /* a kernel's bounded wait expired (see gqa_check_device_errors) */
+} gqa_status;
+
+/* Message for the last non-OK status returned on this thread. */
+const char* gqa_last_error(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int gqa_version(void);
+
+/*
+ * gqa_decode -- FP16 grouped-query attention for one new token per sequence.
+ *
+ * Defined by "NVIDIA SM110 GPU를 위한 실험적인 FP16 GQA 디코드 커널 추가",
+ * section 1 (the sm110_gqa_decode API and its docstring) and section 3 (the
+ * scaled_dot_product_attention comparator with enable_gqa=True):
+ *
+ *   out[b,h,:] = sum_t softmax_t(s) * V[b,g,t,:],   g = h / 4,
+ *   s_t = (q[b,h,:] . K[b,g,t,:]) * q_scale / sqrt(128),   0 <= t < len_b,
+ *   K = kv[b,0,...], V = kv[b,1,...],  len_b = clamp(seq_lens[b], 0, capacity).
+ *
+ *   q         [batch, 32, 128]                 float16
+ *   kv        [batch, 2, 8, capacity, 128]     float16 (K stacked over V)
+ *   seq_lens  [batch]                          int32 (read by the kernels)
+ *   out       [batch, 32, 128]                 float16, written; caller-owned
+ *   batch     1 .. 65535
+ *   capacity  1 .. 2^31 - 1 tokens per sequence
+ *   q_scale   finite; multiplies the standard 1/sqrt(128) scale
+ *
+ * A sequence of length 0 produces a zero row.  Element offsets are computed
+ * in 64-bit, so kv may hold 2^31 or more elements.
+ */
+gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
+                      int64_t capacity, float q_scale, gqa_stream_t stream);
+
+/*
+ * nvfp4_paged_ctx_attn -- paged context (prefill) attention with FP8-E4M3
+ * query and output and NVFP4 K/V pages, bottom-right causal.
+ *
+ * Defined by "GB300 NVFP4 Context Attention: scale slot 조기 반납과 8단 packed
+ * K/V ring", introduction: FP8 (E4M3) query/output, NVFP4 K/V pages with
+ * E4M3 block scales, dequantised to E4M3 in shared memory, head dim 128,
+ * bottom-right causal mask, HND page layout.  For sequence b with
+ * q_len_b = qo_indptr[b+1] - qo_indptr[b] and kv_len_b = kv_lens[b], query i
+ * (row qo_indptr[b] + i) sees key j iff j <= kv_len_b - q_len_b + i, and
+ *
+ *   Kq[b,g,j,d] = E4M3_rne_sat( e2m1(code) * e4m3(scale) )   (same for Vq)
+ *   s_j  = (q[row,h,:] . Kq[b,g,j,:]) * q_scale / sqrt(128),  g = h / 4
+ *   out[row,h,:] = E4M3_rne_sat( (sum_j softmax_j(s) Vq[b,g,j,:]) / out_scale )
+ *
+ *   q_fp8        [total_q, 32, 128]                E4M3 bytes
+ *   k_fp4, v_fp4 [num_pages, 8, 64, 64]            uint8, two E2M1 codes per
+ *                byte, head-dim element 2i in the low nibble of byte i;
+ *                page p, KV head g, slot s holds token 64*p' + s of the
+ *                sequence whose block_table row maps logical page p' to p
+ *   k_sf, v_sf   [num_pages, 8, 64, 8]             E4M3 scale per 16 head-dim
+ *                elements (element d uses scale d / 16)
+ *   block_table  [batch, max_pages_per_seq]        int32 physical page ids;
+ *                entries for logical pages < ceil(kv_len_b / 64) must be in
+ *                [0, num_pages)
+ *   qo_indptr    [batch + 1]                       int32, qo_indptr[0] = 0,
+ *                non-decreasing, qo_indptr[batch] = total_q
+ *   kv_lens      [batch]                           int32, 0 <= kv_len_b <=
+ *                64 * max_pages_per_seq
+ *   out_fp8      [total_q, 32, 128]                E4M3 bytes, written
+ *   q_scale, out_scale  finite, out_scale > 0
+ *
+ * qo_indptr and kv_lens are read on the device only.  A query row that sees
+ * no key (q_len_b > kv_len_b) is written as zeros.  P = softmax numerators
+ * enter the P*V product as E4M3, so the result matches the exact value to
+ * within E4M3 rounding.
+ */
+gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_fp4, const void* k_sf,
+                                const void* v_fp4, const void* v_sf, const int32_t* block_table,
+                                const int32_t* qo_indptr, const int32_t* kv_lens, void* out_fp8,
+                                float out_scale, int64_t batch, int64_t total_q, int64_t num_pages,
+                                int64_t max_pages_per_seq, gqa_stream_t stream);
+
+/*
+ * gqa_debug_dequant_pages -- test export of the context kernel's NVFP4 ->
+ * E4M3 dequantisation (same device routine), gathered through the block
+ * table into a dense array.
+ *
+ *   fp4          [num_pages, 8, 64, 64]   uint8 (as k_fp4 above)
+ *   sf           [num_pages, 8, 64, 8]    E4M3 (as k_sf above)
+ *   block_table  [batch, max_pages_per_seq] int32
+ *   kv_lens      [batch] int32 (device-read)
+ *   out_e4m3     [batch, max_kv, 8, 128]  E4M3 bytes: token t of sequence b
+ *                for t < min(kv_lens[b], max_kv); zero bytes beyond
+ */
+gqa_status gqa_debug_dequant_pages(const void* fp4, const void* sf, const int32_t* block_table,
+                                   const int32_t* kv_lens, void* out_e4m3, int64_t batch, int64_t num_pages,
+                                   int64_t max_pages_per_seq, int64_t max_kv, gqa_stream_t stream);
+
+/*
+ * gqa_check_device_errors -- synchronise `device` and return (then clear)
+ * the kernels' device error word in *word: bit 0 = a bounded wait expired,
+ * bit 1 = an out-of-range page index was skipped.  Returns GQA_ERR_TIMEOUT
+ * when bit 0 is set, GQA_OK when the word is 0.
+ */
+gqa_status gqa_check_device_errors(int device, uint32_t* word);
+
+/* Free every workspace the library holds (all devices and streams).  The
+ * caller must ensure no libgqa work is still running. */
+gqa_status gqa_release_workspace(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_H_ */

@@ -1,0 +1,107 @@
+"""The C ABI: libgqa.so loads, exports every entry point include/gqa.h
+declares, and rejects bad arguments on the host before any CUDA call.
+(No GPU needed: every call here fails validation before touching CUDA.)"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gqa_attention_kv_split_gb300 as gqa
+from gqa_attention_kv_split_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa.h")
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return gqa.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"^(?:const\s+char\s*\*|gqa_status|int)\s+(\w+)\s*\(", src, flags=re.M)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    assert {"gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages", "gqa_last_error",
+            "gqa_check_device_errors", "gqa_release_workspace", "gqa_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"libgqa.so does not export {name}"
+    assert L.gqa_version() >= 100
+
+
+P = ctypes.c_void_p
+
+
+def fake(addr=0x10000):
+    return P(addr)
+
+
+def test_decode_rejects_bad_sizes_and_nulls(L):
+    s = P(0)
+    assert L.gqa_decode(fake(), fake(), fake(), fake(), 0, 16, 1.0, s) == UNSUPPORTED
+    assert b"batch" in L.gqa_last_error()
+    assert L.gqa_decode(fake(), fake(), fake(), fake(), 70000, 16, 1.0, s) == UNSUPPORTED
+    assert L.gqa_decode(fake(), fake(), fake(), fake(), 1, 0, 1.0, s) == UNSUPPORTED
+    assert L.gqa_decode(fake(), fake(), fake(), fake(), 1, 16, float("nan"), s) == INVALID
+    assert L.gqa_decode(fake(), fake(), fake(), fake(), 1, 16, float("inf"), s) == INVALID
+    assert L.gqa_decode(P(0), fake(), fake(), fake(), 1, 16, 1.0, s) == INVALID
+    assert b"q is a null pointer" in L.gqa_last_error()
+    assert L.gqa_decode(fake(), fake(), P(0), fake(), 1, 16, 1.0, s) == INVALID
+    assert b"seq_lens" in L.gqa_last_error()
+
+
+def test_ctx_rejects_bad_sizes_and_nulls(L):
+    s = P(0)
+    f = fake()
+    args = [f, 1.0, f, f, f, f, f, f, f, f, 1.0]
+    assert L.nvfp4_paged_ctx_attn(*args, 0, 16, 4, 2, s) == UNSUPPORTED
+    assert L.nvfp4_paged_ctx_attn(*args, 1, -1, 4, 2, s) == INVALID
+    assert L.nvfp4_paged_ctx_attn(*args, 1, 16, 0, 2, s) == INVALID
+    assert L.nvfp4_paged_ctx_attn(*args, 1, 16, 4, 0, s) == INVALID
+    bad_out = [f, 1.0, f, f, f, f, f, f, f, f, 0.0]
+    assert L.nvfp4_paged_ctx_attn(*bad_out, 1, 16, 4, 2, s) == INVALID
+    assert b"out_scale" in L.gqa_last_error()
+    nan_q = [f, float("nan"), f, f, f, f, f, f, f, f, 1.0]
+    assert L.nvfp4_paged_ctx_attn(*nan_q, 1, 16, 4, 2, s) == INVALID
+    null_kv = [f, 1.0, f, f, f, f, f, f, P(0), f, 1.0]
+    assert L.nvfp4_paged_ctx_attn(*null_kv, 1, 16, 4, 2, s) == INVALID
+    assert b"kv_lens" in L.gqa_last_error()
+
+
+def test_dequant_rejects_bad_sizes(L):
+    s = P(0)
+    f = fake()
+    assert L.gqa_debug_dequant_pages(f, f, f, f, f, 1, 4, 2, 129, s) == INVALID  # max_kv > 64 * pages
+    assert L.gqa_debug_dequant_pages(f, f, f, f, f, 0, 4, 2, 64, s) == UNSUPPORTED
+    assert L.gqa_debug_dequant_pages(f, f, P(0), f, f, 1, 4, 2, 64, s) == INVALID
+
+
+def test_python_binding_raises_without_library(monkeypatch):
+    monkeypatch.setattr(gqa, "_lib", None)
+    monkeypatch.setattr(gqa, "LIB_PATH", "/nonexistent/libgqa.so")
+    import torch
+    with pytest.raises(RuntimeError, match="not built"):
+        gqa.gqa_decode(torch.zeros(1, 32, 128, dtype=torch.float16),
+                       torch.zeros(1, 2, 8, 4, 128, dtype=torch.float16),
+                       torch.ones(1, dtype=torch.int32))
+
+
+def test_python_binding_checks_shapes_and_dtypes():
+    import torch
+    with pytest.raises(TypeError):
+        gqa.gqa_decode(torch.zeros(1, 32, 128), torch.zeros(1, 2, 8, 4, 128, dtype=torch.float16),
+                       torch.ones(1, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        gqa.gqa_decode(torch.zeros(1, 32, 128, dtype=torch.float16),
+                       torch.zeros(1, 2, 4, 4, 128, dtype=torch.float16), torch.ones(1, dtype=torch.int32))
