@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "GqaError", "lib", "gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages",
-    "gqa_check_device_errors", "gqa_release_workspace", "LIB_PATH", "build",
+    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "LIB_PATH", "build",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
             L.gqa_debug_dequant_pages.restype = c.c_int
             L.gqa_check_device_errors.argtypes = [c.c_int, c.POINTER(c.c_uint32)]
             L.gqa_check_device_errors.restype = c.c_int
+            L.gqa_decode_plan.argtypes = [i64, i64, c.POINTER(c.c_int32), c.POINTER(c.c_int32),
+                                          c.POINTER(c.c_int32)]
+            L.gqa_decode_plan.restype = c.c_int
             L.gqa_release_workspace.argtypes = []
             L.gqa_release_workspace.restype = c.c_int
             _lib = L
@@ -168,6 +171,13 @@ def gqa_debug_dequant_pages(fp4, sf, block_table, kv_lens, max_kv: int) -> torch
     _check(lib().gqa_debug_dequant_pages(_p(fp4), _p(sf), _p(block_table), _p(kv_lens), _p(out), B, P,
                                          block_table.shape[1], int(max_kv), _stream_for(fp4)))
     return out
+
+
+def gqa_decode_plan(batch: int, capacity: int) -> dict:
+    """tokens_per_split, num_splits and num_launches of a gqa_decode call."""
+    t, n, l = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().gqa_decode_plan(int(batch), int(capacity), ctypes.byref(t), ctypes.byref(n), ctypes.byref(l)))
+    return {"tokens_per_split": t.value, "num_splits": n.value, "num_launches": l.value}
 
 
 def gqa_check_device_errors(device: int = 0) -> int:

@@ -238,6 +238,18 @@ gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, vo
   return GQA_OK;
 }
 
+gqa_status gqa_decode_plan(int64_t batch, int64_t capacity, int32_t* tokens_per_split, int32_t* num_splits,
+                           int32_t* num_launches) {
+  if (batch < 1 || batch > 65535) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 65535]", (long long)batch);
+  if (capacity < 1 || capacity > 2147483647LL)
+    return fail(GQA_ERR_UNSUPPORTED, "capacity %lld outside [1, 2^31-1]", (long long)capacity);
+  const gqa::DecodePlan plan = gqa::plan_decode(batch, capacity);
+  if (tokens_per_split) *tokens_per_split = plan.chunk;
+  if (num_splits) *num_splits = plan.n_splits;
+  if (num_launches) *num_launches = plan.n_splits > 1 ? 2 : 1;
+  return GQA_OK;
+}
+
 gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_fp4, const void* k_sf,
                                 const void* v_fp4, const void* v_sf, const int32_t* block_table,
                                 const int32_t* qo_indptr, const int32_t* kv_lens, void* out_fp8,

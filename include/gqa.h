@@ -91,6 +91,17 @@ gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, vo
                       int64_t capacity, float q_scale, gqa_stream_t stream);
 
 /*
+ * gqa_decode_plan -- how gqa_decode splits the KV sequence for a given batch
+ * and capacity (chosen from these two only; the lengths stay on the device):
+ * *tokens_per_split tokens per split CTA, *num_splits splits per sequence,
+ * *num_launches kernels per call (1 when one split covers the capacity: the
+ * split kernel then writes the output itself; 2 otherwise: split + merge).
+ * Any output pointer may be NULL.
+ */
+gqa_status gqa_decode_plan(int64_t batch, int64_t capacity, int32_t* tokens_per_split, int32_t* num_splits,
+                           int32_t* num_launches);
+
+/*
  * nvfp4_paged_ctx_attn -- paged context (prefill) attention with FP8-E4M3
  * query and output and NVFP4 K/V pages, bottom-right causal.
  *

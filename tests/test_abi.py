@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
     assert {"gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages", "gqa_last_error",
-            "gqa_check_device_errors", "gqa_release_workspace", "gqa_version"} <= names
+            "gqa_check_device_errors", "gqa_release_workspace", "gqa_version", "gqa_decode_plan"} <= names
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -105,3 +105,14 @@ def test_python_binding_checks_shapes_and_dtypes():
     with pytest.raises(ValueError):
         gqa.gqa_decode(torch.zeros(1, 32, 128, dtype=torch.float16),
                        torch.zeros(1, 2, 4, 4, 128, dtype=torch.float16), torch.ones(1, dtype=torch.int32))
+
+
+def test_decode_plan_covers_capacity():
+    for B, cap in [(2, 256), (64, 8192), (8, 131072), (1, 1), (3, 1000)]:
+        p = gqa.gqa_decode_plan(B, cap)
+        assert p["tokens_per_split"] % 64 == 0
+        assert p["num_splits"] * p["tokens_per_split"] >= cap
+        assert (p["num_splits"] - 1) * p["tokens_per_split"] < cap
+        assert p["num_launches"] == (1 if p["num_splits"] == 1 else 2)
+    with pytest.raises(gqa.GqaError):
+        gqa.gqa_decode_plan(0, 16)
