@@ -111,7 +111,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.perf_counter())
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -124,9 +127,18 @@ class ClockSampler:
                 self.t.join(timeout=2)
 
     def summary(self):
+        """Samples inside the timed region; if that region was shorter than
+        the sampling period, the samples of the preceding second of warm-up
+        (same kernels, same load) are used and the window says so."""
+        t0, t1 = getattr(self, "start", None), getattr(self, "stop", None)
+        window = "timed region"
+        lines = [l for (t, l) in self.lines if t0 is not None and t0 <= t <= t1 + 0.05]
+        if len(lines) < 3 and t0 is not None:
+            lines = [l for (t, l) in self.lines if t0 - 1.0 <= t <= t1 + 0.05]
+            window = "timed region and the preceding 1 s of warm-up"
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -140,9 +152,8 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        under_load = [s for s in sm if s > 0.5 * (mx or max(sm))] or sm
-        return {"sm_mhz": statistics.median(under_load), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "window": window}
 
 
 # -------------------------------------------------------------- distributed --
@@ -228,18 +239,21 @@ def run_gpu(args):
             gqa.nvfp4_paged_ctx_attn(*ctx_args, q_scale=cx.q_scale, out_scale=cx.out_scale, out=ctx_out)
             evs[3].record(stream)
 
-    for _ in range(args.warmup):
-        step(_events(torch, 4))
-    torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
     all_evs = [_events(torch, 4) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        time.sleep(0.3)  # let the sampler start before the GPU is loaded
+        for _ in range(args.warmup):
+            step(_events(torch, 4))
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        clk.mark("start")
         t0 = time.perf_counter()
         for i in range(args.steps):
             step(all_evs[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        clk.mark("stop")
     barrier()
     dec_ms = [e[0].elapsed_time(e[1]) for e in all_evs] if dx is not None else []
     ctx_ms = [e[2].elapsed_time(e[3]) for e in all_evs] if ctx_ok else []
@@ -445,8 +459,8 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="a single named workload from gqa_workloads")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")

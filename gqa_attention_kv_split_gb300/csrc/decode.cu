@@ -408,10 +408,15 @@ cudaError_t ensure_smem_optin(int dev) {
 }  // namespace
 
 DecodePlan plan_decode(int64_t batch, int64_t capacity) {
-  (void)batch;
   DecodePlan p;
   // A split is a whole number of 64-token quanta (4 warps x 16-token stages).
-  int chunk = 512;
+  // Aim for about 4096 split CTAs over the whole capacity (many waves of 2
+  // CTAs per SM on 152 SMs, so ragged lengths balance), with a power-of-two
+  // split between 256 and 4096 tokens: larger splits cut the per-CTA prologue
+  // and the partial-result traffic, smaller ones balance better.
+  const double per_split = (double)batch * kHkv * (double)capacity / 4096.0;
+  int chunk = 256;
+  while (chunk < 4096 && chunk < per_split) chunk *= 2;
   if (const char* env = getenv("GQA_DECODE_SPLIT_TOKENS")) {
     int v = atoi(env);
     if (v >= kChunkQuantum) chunk = v;
