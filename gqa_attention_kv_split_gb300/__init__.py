@@ -21,7 +21,8 @@ import torch
 
 __all__ = [
     "GqaError", "lib", "gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages",
-    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "LIB_PATH", "build",
+    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_decode_noalloc", "LIB_PATH",
+    "build",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.gqa_debug_dequant_pages.restype = c.c_int
             L.gqa_check_device_errors.argtypes = [c.c_int, c.POINTER(c.c_uint32)]
             L.gqa_check_device_errors.restype = c.c_int
+            L.gqa_decode_noalloc.argtypes = [vp, vp, i32p, vp, i64, i64, f32, vp]
+            L.gqa_decode_noalloc.restype = c.c_int
             L.gqa_decode_plan.argtypes = [i64, i64, c.POINTER(c.c_int32), c.POINTER(c.c_int32),
                                           c.POINTER(c.c_int32)]
             L.gqa_decode_plan.restype = c.c_int
@@ -128,6 +131,23 @@ def gqa_decode(q: torch.Tensor, kv: torch.Tensor, seq_lens: torch.Tensor, *, out
         out = torch.empty_like(q)
     _need(out, "out", (torch.float16,), (B, HQ, D))
     _check(lib().gqa_decode(_p(q), _p(kv), _p(seq_lens), _p(out), B, kv.shape[3], float(q_scale), _stream_for(q)))
+    return out
+
+
+def gqa_decode_noalloc(q: torch.Tensor, kv: torch.Tensor, seq_lens: torch.Tensor, *, out: torch.Tensor,
+                       q_scale: float = 1.0) -> torch.Tensor:
+    """gqa_decode without any device allocation (see include/gqa.h): CUDA
+    tensors only, caller-provided `out`, split partials in the library's
+    16 MiB static device array."""
+    B = q.shape[0]
+    _need(q, "q", (torch.float16,), (B, HQ, D))
+    if kv.dim() != 5:
+        raise ValueError("kv must be [batch, 2, 8, capacity, 128]")
+    _need(kv, "kv", (torch.float16,), (B, 2, HKV, kv.shape[3], D))
+    _need(seq_lens, "sequence_lengths", (torch.int32,), (B,))
+    _need(out, "out", (torch.float16,), (B, HQ, D))
+    _check(lib().gqa_decode_noalloc(_p(q), _p(kv), _p(seq_lens), _p(out), B, kv.shape[3], float(q_scale),
+                                    _stream_for(q)))
     return out
 
 

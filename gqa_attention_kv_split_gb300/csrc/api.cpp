@@ -238,6 +238,33 @@ gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, vo
   return GQA_OK;
 }
 
+gqa_status gqa_decode_noalloc(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
+                              int64_t capacity, float q_scale, gqa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (batch < 1 || batch > 65535) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 65535]", (long long)batch);
+  if (capacity < 1 || capacity > 2147483647LL)
+    return fail(GQA_ERR_UNSUPPORTED, "capacity %lld outside [1, 2^31-1]", (long long)capacity);
+  if (!std::isfinite(q_scale)) return fail(GQA_ERR_INVALID_ARG, "q_scale is not finite");
+  Where where;
+  gqa_status st = locate({{q, "q", 16}, {kv, "kv", 16}, {seq_lens, "seq_lens", 4}, {out, "out", 16}}, &where);
+  if (st != GQA_OK) return st;
+  if (where.host)
+    return fail(GQA_ERR_UNSUPPORTED,
+                "gqa_decode_noalloc takes device pointers only (host buffers would need staging memory)");
+  const gqa::DecodePlan plan = gqa::plan_decode(batch, capacity);
+  const size_t need = gqa::decode_workspace_bytes(batch, plan);
+  if (need > gqa::kDecodeStaticScratchBytes)
+    return fail(GQA_ERR_UNSUPPORTED,
+                "batch %lld x capacity %lld needs %zu bytes of split partials; the static scratch holds %zu "
+                "(use gqa_decode)",
+                (long long)batch, (long long)capacity, need, gqa::kDecodeStaticScratchBytes);
+  ScopedDevice sd(where.device);
+  if (!sd.ok()) return fail(GQA_ERR_CUDA, "cannot switch to device %d", where.device);
+  GQA_CUDA_TRY(gqa::launch_decode_static_scratch(q, kv, seq_lens, out, batch, capacity, q_scale, plan, stream),
+               "decode launch (static scratch)");
+  return GQA_OK;
+}
+
 gqa_status gqa_decode_plan(int64_t batch, int64_t capacity, int32_t* tokens_per_split, int32_t* num_splits,
                            int32_t* num_launches) {
   if (batch < 1 || batch > 65535) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 65535]", (long long)batch);

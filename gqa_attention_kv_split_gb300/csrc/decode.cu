@@ -28,6 +28,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -463,6 +464,45 @@ cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// ---- allocation-free variant ---------------------------------------------
+//
+// Scratch for gqa_decode_noalloc: the per-split partials live in this
+// file-scope device array instead of a cudaMalloc'd workspace.  Every GPU
+// that loads the library holds it until the process exits.  In host code the
+// name g_static_scratch is only a stand-in for the symbol, never a device
+// address: the address is looked up once per device (with that device
+// current) by cudaGetSymbolAddress and cached.
+static __device__ __align__(256) uint8_t g_static_scratch[kDecodeStaticScratchBytes];
+
+namespace {
+std::mutex g_static_mu;
+void* g_static_addr[64] = {};
+}  // namespace
+
+cudaError_t launch_decode_static_scratch(const void* q, const void* kv, const int32_t* seq_lens, void* out,
+                                         int64_t batch, int64_t capacity, float q_scale, const DecodePlan& plan,
+                                         cudaStream_t stream) {
+  if (decode_workspace_bytes(batch, plan) > kDecodeStaticScratchBytes) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (g_static_addr[dev] == nullptr) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_static_scratch);
+      if (e != cudaSuccess) return e;
+      g_static_addr[dev] = p;
+    }
+    scratch = g_static_addr[dev];
+  }
+  // The partials need no clearing: the merge reads only the splits that the
+  // split kernel of this same call has written.
+  return launch_decode(q, kv, seq_lens, out, batch, capacity, q_scale, plan, scratch, stream);
 }
 
 cudaError_t decode_read_errors(uint32_t* word) {

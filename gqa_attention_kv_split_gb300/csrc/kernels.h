@@ -26,6 +26,18 @@ cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens
                           int64_t capacity, float q_scale, const DecodePlan& plan, void* workspace,
                           cudaStream_t stream);
 
+// Size of the file-scope device array that gqa_decode_noalloc uses for the
+// per-split partials (16 MiB per GPU that loads the library).
+constexpr size_t kDecodeStaticScratchBytes = size_t(16) << 20;
+
+// launch_decode with the partials in that static array.  On the first call
+// on a device (which must be current) it looks up the array's device address
+// with cudaGetSymbolAddress and caches it.  Returns cudaErrorInvalidValue if
+// the plan needs more than kDecodeStaticScratchBytes.  Allocates nothing.
+cudaError_t launch_decode_static_scratch(const void* q, const void* kv, const int32_t* seq_lens, void* out,
+                                         int64_t batch, int64_t capacity, float q_scale, const DecodePlan& plan,
+                                         cudaStream_t stream);
+
 // Reads and clears the decode kernels' device error word on the current
 // device (synchronises the device).
 cudaError_t decode_read_errors(uint32_t* word);

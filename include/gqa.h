@@ -91,6 +91,37 @@ gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, vo
                       int64_t capacity, float q_scale, gqa_stream_t stream);
 
 /*
+ * gqa_decode_noalloc -- gqa_decode that allocates no memory.  (An addition
+ * of this library; the pages have no counterpart.)
+ *
+ * Same operation, arguments, layouts and results as gqa_decode, for callers
+ * that cannot allocate device memory at call time: engines that reserve
+ * nearly all of HBM up front for their KV cache and own every byte through
+ * their own allocator (a late cudaMalloc would fail or fragment it), and
+ * latency-critical loops that must not block in cudaMalloc/cudaFree, which
+ * can synchronise the device.  The split partials go to a file-scope device
+ * array of 16 MiB instead of the library workspace; every GPU that loads
+ * libgqa holds that array until the process exits.
+ *
+ *   - Device pointers only (host buffers would need staging memory):
+ *     GQA_ERR_UNSUPPORTED otherwise.
+ *   - Rejects, with GQA_ERR_UNSUPPORTED and a message naming the sizes, a
+ *     (batch, capacity) whose partials exceed 16 MiB: batch * 32 * splits *
+ *     520 bytes, splits as reported by gqa_decode_plan.  The benchmark shapes
+ *     (64 x 8192, 8 x 131072) need 8.5 MB.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind (nothing in it needs to start at zero).  Calls whose kernels
+ *     overlap on the GPU -- on different streams, without ordering -- race on
+ *     it; order them on one stream or with events.
+ *   - Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+gqa_status gqa_decode_noalloc(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
+                              int64_t capacity, float q_scale, gqa_stream_t stream);
+
+/*
  * gqa_decode_plan -- how gqa_decode splits the KV sequence for a given batch
  * and capacity (chosen from these two only; the lengths stay on the device):
  * *tokens_per_split tokens per split CTA, *num_splits splits per sequence,
