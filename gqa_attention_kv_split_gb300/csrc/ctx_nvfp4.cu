@@ -1,18 +1,55 @@
-// ctx_nvfp4.cu -- NVFP4 paged context attention for sm_103a, and the test
-// export of its dequantisation.
+// ctx_nvfp4.cu -- NVFP4 paged context (prefill) attention for sm_103a, and
+// the test export of its dequantisation.
+//
+// Operation ("GB300 NVFP4 Context Attention: scale slot 조기 반납과 8단 packed
+// K/V ring", introduction): FP8-E4M3 query and output, NVFP4 K/V pages in HND
+// layout with E4M3 block scales, dequantised to E4M3 in shared memory, head
+// dim 128, bottom-right causal mask.  For sequence b, query i sees key j iff
+// j <= kv_len - q_len + i;  O = softmax(q K^T * q_scale / sqrt(128)) V, and
+// out = E4M3(O / out_scale).
+//
+// Design (the page's Cake schedule -- 512 threads, 8-stage packed ring, early
+// scale-slot release -- is prior art; this is our own GB300 layout):
+//  * Work unit = (sequence b, KV head g, block of 64 queries).  The 4 query
+//    heads of the group are stacked into the MMA's M dimension: M-tile T
+//    (T = 0, 1) holds queries 32T..32T+31 of the block x 4 heads, row
+//    r = 4 * query + head.  One dequantised K/V tile therefore feeds 256 rows.
+//  * TMEM (512 columns): S_0, S_1, O_0, O_1, 128 fp32 columns each.
+//  * Warp roles (16 warps): 0 = bulk-copy producer of packed NVFP4 pages +
+//    scales through the block table into a 4-stage ring; 1 = TMEM owner and
+//    single-thread tcgen05 MMA issuer; 2-3 = Q loaders (swizzled E4M3 tiles);
+//    4-7 and 8-11 = softmax of M-tile 0 and 1 (one thread per TMEM lane =
+//    row); 12-15 = dequantisers writing E4M3 K and V tiles in the 128-byte
+//    swizzled layout the MMA descriptors read (K as the K-major B operand of
+//    S = Q K^T, V as the MN-major B operand of O = P V).
+//  * MMA order per KV tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  A commit
+//    after S_T(j+1) also covers PV_T(j), so a softmax warp that sees S_T(j+1)
+//    may rescale O_T and overwrite P_T without a further barrier.
+//  * Online softmax in the exp2 domain with a lazy running maximum: the
+//    maximum used for P is raised only when a row's maximum grows by more
+//    than 2^8, so P <= 256 stays inside E4M3 and O is rescaled rarely.  The
+//    row sum accumulates the E4M3-rounded P that the MMA consumes.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
 #include "nvfp4.cuh"
+#include "tcgen05.cuh"
 
 namespace gqa {
 namespace {
 
 __device__ uint32_t g_ctx_err;
 
-// Dense gather of dequantised tokens: one thread per (token, KV head,
-// 16-element block).  Uses the same dequant16 as the attention kernel.
+// ---------------------------------------------------------------------------
+// Debug export: dense gather of dequantised tokens, one thread per (token,
+// KV head, 16-element block), through the same dequant16 as the kernel.
+// ---------------------------------------------------------------------------
 __global__ void dequant_pages_kernel(const uint8_t* __restrict__ fp4, const uint8_t* __restrict__ sf,
                                      const int32_t* __restrict__ block_table, const int32_t* __restrict__ kv_lens,
                                      uint8_t* __restrict__ out, int64_t num_pages, int64_t max_pages_per_seq,
@@ -39,6 +76,419 @@ __global__ void dequant_pages_kernel(const uint8_t* __restrict__ fp4, const uint
   *reinterpret_cast<uint4*>(out + (((int64_t)b * max_kv + t) * kHkv + g) * kD + blk * 16) = r;
 }
 
+// ---------------------------------------------------------------------------
+// Context attention kernel.
+// ---------------------------------------------------------------------------
+constexpr int kQB = 64;                    // queries per work unit
+constexpr int kQT = 32;                    // queries per M=128 tile (x 4 heads)
+constexpr int kKT = 128;                   // keys per KV tile (two pages)
+constexpr int kNP = 4;                     // packed-page ring stages
+constexpr int kCtxThreads = 512;
+constexpr int kTile = 128 * 128;           // one 128 x 128 E4M3 tile: 16 KB
+constexpr int kPackedPage = kPage * kD / 2;   // 4 KB of codes per (page, KV head)
+constexpr int kScalePage = kPage * kD / 16;   // 512 B of scales per (page, KV head)
+constexpr float kRescaleLog2 = 8.f;        // lazy-maximum threshold (P <= 2^8)
+constexpr uint32_t kTmemCols = 512;
+
+struct CtxSmem {
+  uint8_t q[2][kTile];   // M-tiles 0/1 of Q       (128B-swizzled, K-major)
+  uint8_t k[2][kTile];   // E4M3 K, two slots      (128B-swizzled, K-major B operand)
+  uint8_t v[2][kTile];   // E4M3 V, two slots      (128B-swizzled, MN-major B operand)
+  uint8_t p[2][kTile];   // E4M3 P of M-tiles 0/1  (128B-swizzled, K-major A operand)
+  uint8_t pk[kNP][2][2][kPackedPage];  // [stage][K=0,V=1][page of the tile][slot*64 + byte]
+  uint8_t sf[kNP][2][2][kScalePage];   // [stage][K,V][page][slot*8 + block]
+  uint64_t pk_full[kNP], pk_empty[kNP];
+  uint64_t k_ready[2], v_ready[2], kv_free[2];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_final, q_ready;
+  uint32_t tmem_base;
+  int unit_b, unit_qb;
+};
+constexpr size_t kCtxSmemBytes = sizeof(CtxSmem) + 1024;  // + alignment slack
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a 128B-swizzled tile
+  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Work index t -> (b, query block), longest first: rounds r = 0, 1, ...; in
+// round r every sequence with more than r query blocks contributes its block
+// (n_blocks - 1 - r), in batch order.  All lanes of the calling warp get the
+// same answer; b = -1 when t is past the last unit.
+__device__ void find_unit(const int32_t* __restrict__ qo, int B, int t, int& out_b, int& out_qb) {
+  const int lane = threadIdx.x & 31;
+  out_b = -1;
+  out_qb = -1;
+  for (int r = 0;; ++r) {
+    int cnt = 0;
+    bool any = false;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      int nqb = 0;
+      if (b < B) {
+        const int ql = qo[b + 1] - qo[b];
+        nqb = ql > 0 ? (ql + kQB - 1) / kQB : 0;
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, nqb > r);
+      const int c = __popc(bal);
+      if (t >= cnt && t < cnt + c) {
+        unsigned m = bal;
+        for (int i = 0; i < t - cnt; ++i) m &= m - 1;  // drop the lower set bits
+        const int bb = b0 + __ffs(m) - 1;
+        const int ql = qo[bb + 1] - qo[bb];
+        out_b = bb;
+        out_qb = (ql + kQB - 1) / kQB - 1 - r;
+        return;
+      }
+      cnt += c;
+      any |= (bal != 0u);
+    }
+    if (!any) return;
+    t -= cnt;
+  }
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// Two floats -> two E4M3 bytes (x in the low byte), RNE, satfinite.
+__device__ __forceinline__ uint32_t f2_to_e4m3x2(float lo, float hi) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Two E4M3 bytes (low 16 bits) -> their values.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+__global__ void __launch_bounds__(kCtxThreads, 1)
+    ctx_nvfp4_kernel(const CtxArgs a, const float scale_log2, const float inv_out_scale) {
+  extern __shared__ uint8_t smem_raw[];
+  CtxSmem& sm = *reinterpret_cast<CtxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = blockIdx.x % kHkv;
+
+  if (warp == 0) {
+    int ub, uqb;
+    find_unit(a.qo_indptr, (int)a.batch, (int)(blockIdx.x / kHkv), ub, uqb);
+    if (lane == 0) {
+      sm.unit_b = ub;
+      sm.unit_qb = uqb;
+    }
+  }
+  if (threadIdx.x == 32) {
+    for (int i = 0; i < kNP; ++i) {
+      mbar_init(smem_u32(&sm.pk_full[i]), 1);
+      mbar_init(smem_u32(&sm.pk_empty[i]), 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sm.k_ready[i]), 4);
+      mbar_init(smem_u32(&sm.v_ready[i]), 4);
+      mbar_init(smem_u32(&sm.kv_free[i]), 1);
+      mbar_init(smem_u32(&sm.s_full[i]), 1);
+      mbar_init(smem_u32(&sm.p_full[i]), 4);
+    }
+    mbar_init(smem_u32(&sm.o_final), 1);
+    mbar_init(smem_u32(&sm.q_ready), 2);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int b = sm.unit_b;
+  if (b < 0) return;  // past the last unit: the whole CTA leaves
+  const int qb = sm.unit_qb;
+  const int qo = a.qo_indptr[b];
+  const int q_len = a.qo_indptr[b + 1] - qo;
+  int kv_len = a.kv_lens[b];
+  const int kv_cap = (int)(a.max_pages_per_seq * kPage);
+  kv_len = kv_len < 0 ? 0 : (kv_len > kv_cap ? kv_cap : kv_len);
+  const int q0 = qb * kQB;
+  const int q_last = min(q0 + kQB, q_len) - 1;
+  const int n_keys = min(kv_len, kv_len - q_len + q_last + 1);
+  const int n_tiles = n_keys > 0 ? (n_keys + kKT - 1) / kKT : 0;
+
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_thread_sync();
+  __syncthreads();
+  tc::fence_after_thread_sync();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_tiles > 0) {
+      const uint64_t pol = policy_evict_last();  // pages are re-read by the other query blocks
+      const int n_pages = (kv_len + kPage - 1) / kPage;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j % kNP;
+        if (j >= kNP && !mbar_wait(smem_u32(&sm.pk_empty[st]), ((j / kNP) - 1) & 1, &g_ctx_err)) break;
+        const int np = min(2, n_pages - 2 * j);
+        const uint32_t fb = smem_u32(&sm.pk_full[st]);
+        mbar_arrive_expect_tx(fb, (uint32_t)np * 2u * (kPackedPage + kScalePage));
+        for (int h = 0; h < np; ++h) {
+          int phys = a.block_table[(int64_t)b * a.max_pages_per_seq + 2 * j + h];
+          if (phys < 0 || phys >= a.num_pages) {
+            atomicOr(&g_ctx_err, kErrBadIndex);
+            phys = 0;
+          }
+          const int64_t row = ((int64_t)phys * kHkv + g) * kPage;
+          bulk_g2s_hint(smem_u32(sm.pk[st][0][h]), a.k_fp4 + row * (kD / 2), kPackedPage, fb, pol);
+          bulk_g2s_hint(smem_u32(sm.sf[st][0][h]), a.k_sf + row * (kD / 16), kScalePage, fb, pol);
+          bulk_g2s_hint(smem_u32(sm.pk[st][1][h]), a.v_fp4 + row * (kD / 2), kPackedPage, fb, pol);
+          bulk_g2s_hint(smem_u32(sm.sf[st][1][h]), a.v_sf + row * (kD / 16), kScalePage, fb, pol);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t idS = tc::idesc_e4m3_f32(128, 128, false);  // B = K tile, K-major
+      constexpr uint32_t idO = tc::idesc_e4m3_f32(128, 128, true);   // B = V tile, MN-major
+      const uint32_t q_base = smem_u32(sm.q[0]);
+      const uint32_t k_base = smem_u32(sm.k[0]);
+      const uint32_t v_base = smem_u32(sm.v[0]);
+      const uint32_t p_base = smem_u32(sm.p[0]);
+      auto issue_s = [&](int T, int slot) {
+        const uint32_t qa = q_base + (uint32_t)T * kTile;
+        const uint32_t ka = k_base + (uint32_t)slot * kTile;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_e4m3(tmem + T * 128, tc::sw128_desc(qa + 32 * k), tc::sw128_desc(ka + 32 * k), idS, k > 0);
+      };
+      auto issue_pv = [&](int T, int slot, bool acc) {
+        const uint32_t pa = p_base + (uint32_t)T * kTile;
+        const uint32_t va = v_base + (uint32_t)slot * kTile;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_e4m3(tmem + 256 + T * 128, tc::sw128_desc(pa + 32 * k), tc::sw128_desc(va + 4096 * k), idO,
+                       (acc || k > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(smem_u32(&sm.q_ready), 0, &g_ctx_err) &&
+                mbar_wait(smem_u32(&sm.k_ready[0]), 0, &g_ctx_err);
+      if (ok) {
+        tc::fence_after_thread_sync();
+        issue_s(0, 0);
+        tc::commit(smem_u32(&sm.s_full[0]));
+        issue_s(1, 0);
+        tc::commit(smem_u32(&sm.s_full[1]));
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int slot = j & 1;
+        for (int T = 0; T < 2 && ok; ++T) {
+          ok = mbar_wait(smem_u32(&sm.p_full[T]), j & 1, &g_ctx_err);
+          if (ok && T == 0) ok = mbar_wait(smem_u32(&sm.v_ready[slot]), (j >> 1) & 1, &g_ctx_err);
+          if (!ok) break;
+          tc::fence_after_thread_sync();
+          issue_pv(T, slot, j > 0);
+          if (T == 1) tc::commit(smem_u32(&sm.kv_free[slot]));
+          if (j + 1 < n_tiles) {
+            if (T == 0) {
+              ok = mbar_wait(smem_u32(&sm.k_ready[(j + 1) & 1]), ((j + 1) >> 1) & 1, &g_ctx_err);
+              if (!ok) break;
+              tc::fence_after_thread_sync();
+            }
+            issue_s(T, (j + 1) & 1);
+            tc::commit(smem_u32(&sm.s_full[T]));
+          }
+        }
+      }
+      tc::commit(smem_u32(&sm.o_final));
+    }
+  } else if (warp < 4) {
+    // ----------------------------------------------------------- Q loaders
+    const int lt = threadIdx.x - 64;
+    for (int i = lt; i < 2 * 128 * 8; i += 64) {
+      const int T = i >> 10;
+      const int r = (i >> 3) & 127;
+      const int c = i & 7;
+      const int qrow = q0 + T * kQT + (r >> 2);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (qrow < q_len)
+        v = *reinterpret_cast<const uint4*>(a.q + ((int64_t)(qo + qrow) * kHq + g * kGroup + (r & 3)) * kD + c * 16);
+      *reinterpret_cast<uint4*>(sm.q[T] + swz(r, c)) = v;
+    }
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm.q_ready));
+  } else if (warp < 12) {
+    // -------------------------------------------------------------- softmax
+    const int T = (warp - 4) >> 2;
+    const int sub = warp & 3;
+    const int r = 32 * sub + lane;  // TMEM lane = row of M-tile T
+    const int qrow = q0 + T * kQT + (r >> 2);
+    const int hh = r & 3;
+    int lim = kv_len - q_len + qrow;  // last visible key (inclusive)
+    if (lim > kv_len - 1) lim = kv_len - 1;
+    const uint32_t lane_off = (uint32_t)(32 * sub) << 16;
+    const uint32_t tS = tmem + lane_off + (uint32_t)(T * 128);
+    const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(T * 128);
+    uint8_t* prow = sm.p[T];
+    float m_used = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      // warp-uniform outcome: the TMEM accesses below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[T]), j & 1, &g_ctx_err))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_thread_sync();
+      const int kbase = j * kKT;
+      const bool masked = kbase + kKT - 1 > lim;
+      // pass 1: row maximum of the scaled logits
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tc::ld32(tS + 32 * c, v);
+        tc::ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float x = u2f(v[i]) * scale_log2;
+          if (masked && kbase + 32 * c + i > lim) x = -INFINITY;
+          mx = fmaxf(mx, x);
+        }
+      }
+      const float m_new = fmaxf(m_used, mx);
+      const bool raise = m_new > m_used + kRescaleLog2;  // also true for the first finite maximum
+      const float alpha = raise ? exp2f(m_used - m_new) : 1.f;  // 0 when m_used was -inf
+      if (__any_sync(0xffffffffu, raise && j > 0)) {
+        // O_T holds PV of tiles < j (complete: this S_T(j) was committed after them)
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tc::ld32(tO + 32 * c, o);
+          tc::ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(u2f(o[i]) * alpha);
+          tc::st32(tO + 32 * c, o);
+        }
+        tc::st_wait();
+      }
+      if (raise) {
+        l *= alpha;
+        m_used = m_new;
+      }
+      const bool dead = (m_used == -INFINITY);  // no visible key yet
+      // pass 2: P = 2^(x - m_used) as E4M3 into the swizzled P tile
+      float lsum = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tc::ld32(tS + 32 * c, v);
+        tc::ld_wait();
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int k0 = kbase + 32 * c + 2 * i;
+          float p0 = fast_exp2(fmaf(u2f(v[2 * i]), scale_log2, -m_used));
+          float p1 = fast_exp2(fmaf(u2f(v[2 * i + 1]), scale_log2, -m_used));
+          if (dead || (masked && k0 > lim)) p0 = 0.f;
+          if (dead || (masked && k0 + 1 > lim)) p1 = 0.f;
+          const uint32_t e = f2_to_e4m3x2(p0, p1);
+          const float2 back = e4m3x2_to_f2(e);
+          lsum += back.x + back.y;
+          if (i & 1)
+            pk[i >> 1] |= e << 16;
+          else
+            pk[i >> 1] = e;
+        }
+        *reinterpret_cast<uint4*>(prow + swz(r, 2 * c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(prow + swz(r, 2 * c + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+      l += lsum;
+      tc::fence_proxy_async_smem();
+      tc::fence_before_thread_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[T]));
+    }
+    // ------------------------------------------------------------ epilogue
+    bool have_o = false;
+    if (ok && n_tiles > 0) {
+      have_o = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_final), 0, &g_ctx_err));
+      tc::fence_after_thread_sync();
+    }
+    const float inv = (l > 0.f) ? inv_out_scale / l : 0.f;
+    uint8_t* dst = a.out + ((int64_t)(qo + qrow) * kHq + g * kGroup + hh) * kD;
+    const bool store = qrow < q_len;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      if (have_o) {
+        tc::ld32(tO + 32 * c, o);
+        tc::ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = f2_to_e4m3x2(u2f(o[4 * i]) * inv, u2f(o[4 * i + 1]) * inv);
+        const uint32_t hi = f2_to_e4m3x2(u2f(o[4 * i + 2]) * inv, u2f(o[4 * i + 3]) * inv);
+        pk[i] = lo | (hi << 16);
+      }
+      if (store) {
+        *reinterpret_cast<uint4*>(dst + 32 * c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(dst + 32 * c + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- dequantisers
+    const int dt = threadIdx.x - 384;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j % kNP;
+      const int slot = j & 1;
+      if (!mbar_wait(smem_u32(&sm.pk_full[st]), (j / kNP) & 1, &g_ctx_err)) break;
+      if (j >= 2 && !mbar_wait(smem_u32(&sm.kv_free[slot]), ((j >> 1) - 1) & 1, &g_ctx_err)) break;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        uint8_t* dst = kv == 0 ? sm.k[slot] : sm.v[slot];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int i = dt + 128 * it;  // item = (key, 16-element block)
+          const int key = i >> 3;
+          const int blk = i & 7;
+          uint4 out = make_uint4(0u, 0u, 0u, 0u);
+          if (j * kKT + key < kv_len) {
+            const int h = key >> 6;
+            const int s = key & 63;
+            const uint2 packed = *reinterpret_cast<const uint2*>(&sm.pk[st][kv][h][s * 64 + blk * 8]);
+            out = dequant16(packed, sm.sf[st][kv][h][s * 8 + blk]);
+          }
+          *reinterpret_cast<uint4*>(dst + swz(key, blk)) = out;
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(kv == 0 ? &sm.k_ready[slot] : &sm.v_ready[slot]));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.pk_empty[st]));
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc::fence_before_thread_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_thread_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+std::atomic<uint64_t> g_ctx_smem_ready{0};
+
+cudaError_t ensure_ctx_smem(int dev) {
+  const uint64_t bit = 1ull << (dev & 63);
+  if (g_ctx_smem_ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  cudaError_t e =
+      cudaFuncSetAttribute(ctx_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCtxSmemBytes);
+  if (e != cudaSuccess) return e;
+  g_ctx_smem_ready.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_dequant_pages(const uint8_t* fp4, const uint8_t* sf, const int32_t* block_table,
@@ -52,9 +502,18 @@ cudaError_t launch_dequant_pages(const uint8_t* fp4, const uint8_t* sf, const in
 }
 
 cudaError_t launch_ctx(const CtxArgs& a, cudaStream_t stream) {
-  (void)a;
-  (void)stream;
-  return cudaErrorNotSupported;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = ensure_ctx_smem(dev)) != cudaSuccess) return e;
+  // Upper bound on the number of (sequence, 64-query block) units without
+  // reading qo_indptr on the host: sum_b ceil(q_len_b / 64) <= total_q / 64 + batch.
+  const int64_t blocks = (a.total_q + kQB - 1) / kQB + a.batch;
+  const int64_t grid = blocks * kHkv;
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const float scale_log2 = a.q_scale / sqrtf((float)kD) * 1.4426950408889634f;
+  ctx_nvfp4_kernel<<<(unsigned)grid, kCtxThreads, kCtxSmemBytes, stream>>>(a, scale_log2, 1.f / a.out_scale);
+  return cudaGetLastError();
 }
 
 cudaError_t ctx_read_errors(uint32_t* word) {
