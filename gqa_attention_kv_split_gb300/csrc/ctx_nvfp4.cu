@@ -25,10 +25,16 @@
 //  * MMA order per KV tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  A commit
 //    after S_T(j+1) also covers PV_T(j), so a softmax warp that sees S_T(j+1)
 //    may rescale O_T and overwrite P_T without a further barrier.
-//  * Online softmax in the exp2 domain with a lazy running maximum: the
-//    maximum used for P is raised only when a row's maximum grows by more
-//    than 2^8, so P <= 256 stays inside E4M3 and O is rescaled rarely.  The
-//    row sum accumulates the E4M3-rounded P that the MMA consumes.
+//  * Online softmax in the exp2 domain with a lazy running maximum m: m is
+//    raised only when a row's maximum exceeds it by more than 2^4, so O is
+//    rescaled rarely.  P = 2^(x - m + 4) <= 2^8 stays inside E4M3, and the
+//    +4 lifts the weights that matter out of E4M3's subnormal range (below
+//    2^-6), where a split term would lose its relative precision.
+//  * P enters the FP8 PV product as two E4M3 terms, P_hi = E4M3(P) and
+//    P_lo = E4M3(P - P_hi), each multiplied by V into the same TMEM
+//    accumulator.  One E4M3 term alone carries ~2 % relative error per
+//    weight, which shows in the output after its own E4M3 rounding; the
+//    pair carries ~2^-8.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -82,19 +88,21 @@ __global__ void dequant_pages_kernel(const uint8_t* __restrict__ fp4, const uint
 constexpr int kQB = 64;                    // queries per work unit
 constexpr int kQT = 32;                    // queries per M=128 tile (x 4 heads)
 constexpr int kKT = 128;                   // keys per KV tile (two pages)
-constexpr int kNP = 4;                     // packed-page ring stages
+constexpr int kNP = 3;                     // packed-page ring stages
 constexpr int kCtxThreads = 512;
 constexpr int kTile = 128 * 128;           // one 128 x 128 E4M3 tile: 16 KB
 constexpr int kPackedPage = kPage * kD / 2;   // 4 KB of codes per (page, KV head)
 constexpr int kScalePage = kPage * kD / 16;   // 512 B of scales per (page, KV head)
-constexpr float kRescaleLog2 = 8.f;        // lazy-maximum threshold (P <= 2^8)
+constexpr float kRescaleLog2 = 4.f;        // lazy-maximum threshold
+constexpr float kPBiasLog2 = 4.f;          // P = 2^(x - m + 4): P <= 2^(4 + 4) = 256 < 448
 constexpr uint32_t kTmemCols = 512;
 
 struct CtxSmem {
   uint8_t q[2][kTile];   // M-tiles 0/1 of Q       (128B-swizzled, K-major)
   uint8_t k[2][kTile];   // E4M3 K, two slots      (128B-swizzled, K-major B operand)
   uint8_t v[2][kTile];   // E4M3 V, two slots      (128B-swizzled, MN-major B operand)
-  uint8_t p[2][kTile];   // E4M3 P of M-tiles 0/1  (128B-swizzled, K-major A operand)
+  uint8_t p[2][kTile];   // E4M3 P_hi of M-tiles 0/1 (128B-swizzled, K-major A operand)
+  uint8_t pl[2][kTile];  // E4M3 P_lo = E4M3(P - P_hi) of M-tiles 0/1
   uint8_t pk[kNP][2][2][kPackedPage];  // [stage][K=0,V=1][page of the tile][slot*64 + byte]
   uint8_t sf[kNP][2][2][kScalePage];   // [stage][K,V][page][slot*8 + block]
   uint64_t pk_full[kNP], pk_empty[kNP];
@@ -154,10 +162,16 @@ __device__ __forceinline__ uint32_t f2_to_e4m3x2(float lo, float hi) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Two E4M3 bytes (low 16 bits) -> their values.
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+// (p0, p1) -> hi = E4M3(p) and lo = E4M3(p - hi), two bytes each (p0 low).
+// p is first rounded to f16 (11 significant bits); hi and lo are taken from
+// that value, and the difference f16(p) - hi is exact in f16 (hi lies within
+// a factor 1 +- 2^-4 of it, or both sit on the 2^-9 subnormal grid).
+__device__ __forceinline__ void split_e4m3x2(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  const __half2 ph = __floats2half2_rn(p0, p1);
+  hi = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&ph));
+  const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)hi, __NV_E4M3);
+  const __half2 d = __hsub2(ph, *reinterpret_cast<const __half2*>(&hb));
+  lo = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&d));
 }
 
 __global__ void __launch_bounds__(kCtxThreads, 1)
@@ -256,13 +270,17 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         for (int k = 0; k < 4; ++k)
           tc::mma_e4m3(tmem + T * 128, tc::sw128_desc(qa + 32 * k), tc::sw128_desc(ka + 32 * k), idS, k > 0);
       };
+      const uint32_t pl_base = smem_u32(sm.pl[0]);
       auto issue_pv = [&](int T, int slot, bool acc) {
         const uint32_t pa = p_base + (uint32_t)T * kTile;
+        const uint32_t pla = pl_base + (uint32_t)T * kTile;
         const uint32_t va = v_base + (uint32_t)slot * kTile;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 4; ++k) {
           tc::mma_e4m3(tmem + 256 + T * 128, tc::sw128_desc(pa + 32 * k), tc::sw128_desc(va + 4096 * k), idO,
                        (acc || k > 0) ? 1u : 0u);
+          tc::mma_e4m3(tmem + 256 + T * 128, tc::sw128_desc(pla + 32 * k), tc::sw128_desc(va + 4096 * k), idO, 1u);
+        }
       };
       bool ok = mbar_wait(smem_u32(&sm.q_ready), 0, &g_ctx_err) &&
                 mbar_wait(smem_u32(&sm.k_ready[0]), 0, &g_ctx_err);
@@ -324,6 +342,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     const uint32_t tS = tmem + lane_off + (uint32_t)(T * 128);
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(T * 128);
     uint8_t* prow = sm.p[T];
+    uint8_t* plrow = sm.pl[T];
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
@@ -371,31 +390,37 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         m_used = m_new;
       }
       const bool dead = (m_used == -INFINITY);  // no visible key yet
-      // pass 2: P = 2^(x - m_used) as E4M3 into the swizzled P tile
+      const float m_off = m_used - kPBiasLog2;
+      // pass 2: P = 2^(x - m_used) as two E4M3 terms into the swizzled P tiles
       float lsum = 0.f;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
         tc::ld32(tS + 32 * c, v);
         tc::ld_wait();
-        uint32_t pk[8];
+        uint32_t ph[8], pl[8];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int k0 = kbase + 32 * c + 2 * i;
-          float p0 = fast_exp2(fmaf(u2f(v[2 * i]), scale_log2, -m_used));
-          float p1 = fast_exp2(fmaf(u2f(v[2 * i + 1]), scale_log2, -m_used));
+          float p0 = fast_exp2(fmaf(u2f(v[2 * i]), scale_log2, -m_off));
+          float p1 = fast_exp2(fmaf(u2f(v[2 * i + 1]), scale_log2, -m_off));
           if (dead || (masked && k0 > lim)) p0 = 0.f;
           if (dead || (masked && k0 + 1 > lim)) p1 = 0.f;
-          const uint32_t e = f2_to_e4m3x2(p0, p1);
-          const float2 back = e4m3x2_to_f2(e);
-          lsum += back.x + back.y;
-          if (i & 1)
-            pk[i >> 1] |= e << 16;
-          else
-            pk[i >> 1] = e;
+          lsum += p0 + p1;
+          uint32_t hi, lo;
+          split_e4m3x2(p0, p1, hi, lo);
+          if (i & 1) {
+            ph[i >> 1] |= hi << 16;
+            pl[i >> 1] |= lo << 16;
+          } else {
+            ph[i >> 1] = hi;
+            pl[i >> 1] = lo;
+          }
         }
-        *reinterpret_cast<uint4*>(prow + swz(r, 2 * c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(prow + swz(r, 2 * c + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        *reinterpret_cast<uint4*>(prow + swz(r, 2 * c)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        *reinterpret_cast<uint4*>(prow + swz(r, 2 * c + 1)) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
+        *reinterpret_cast<uint4*>(plrow + swz(r, 2 * c)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        *reinterpret_cast<uint4*>(plrow + swz(r, 2 * c + 1)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
       }
       l += lsum;
       tc::fence_proxy_async_smem();

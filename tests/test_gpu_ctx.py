@@ -87,7 +87,7 @@ def test_deterministic_and_host_path():
 def test_workload_b4_q2048_kv2048_full():
     x = W.ctx_workload("ctx_b4_q2048_kv2048")
     frac, rl, mx = check_ctx(run(x), ref(x), "ctx_b4_q2048_kv2048")
-    print(f"within-2-ulp fraction {frac:.6f}, rel-L2 {rl:.3e}, max ulps {mx}")
+    assert rl <= 3e-2  # attainable here: the plain bound applies
 
 
 def test_workload_b2_q4096_kv65536_sampled():
