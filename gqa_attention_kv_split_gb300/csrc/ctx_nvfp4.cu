@@ -14,33 +14,40 @@
 //    heads of the group are stacked into the MMA's M dimension: M-tile T
 //    (T = 0, 1) holds queries 32T..32T+31 of the block x 4 heads, row
 //    r = 4 * query + head.  One dequantised K/V tile therefore feeds 256 rows.
-//  * TMEM (512 columns): S_0, S_1, O_0, O_1, 128 fp32 columns each.
+//  * KV tiles of 64 keys (one page).  TMEM (512 columns) per M-tile T: two
+//    S buffers of 64 fp32 columns (S of tile j in buffer j & 1) and O (128
+//    columns), so the MMA computes S(j+2) while the softmax works on tile
+//    j+1.  P is written back over the consumed S columns and read from TMEM
+//    as the A operand of PV.
 //  * Warp roles (16 warps): 0 = bulk-copy producer of packed NVFP4 pages +
-//    scales through the block table into a 4-stage ring; 1 = TMEM owner and
-//    single-thread tcgen05 MMA issuer; 2-3 = Q loaders (swizzled E4M3 tiles);
+//    scales through the block table into a 6-stage ring; 1 = TMEM owner and
+//    single-thread tcgen05 MMA issuer; 2 = Q loader (two TMA boxes through a
+//    128-byte-swizzling tensor map); 3 = idle;
 //    4-7 and 8-11 = softmax of M-tile 0 and 1 (one thread per TMEM lane =
 //    row); 12-15 = dequantisers writing E4M3 K and V tiles in the 128-byte
 //    swizzled layout the MMA descriptors read (K as the K-major B operand of
 //    S = Q K^T, V as the MN-major B operand of O = P V).
-//  * MMA order per KV tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  A commit
-//    after S_T(j+1) also covers PV_T(j), so a softmax warp that sees S_T(j+1)
-//    may rescale O_T and overwrite P_T without a further barrier.
+//  * MMA order per KV tile j: PV_0(j), S_0(j+2), PV_1(j), S_1(j+2).  A
+//    softmax warp that raises its running maximum waits for the PV of the
+//    previous tile (o_done) before rescaling O in TMEM.
 //  * Online softmax in the exp2 domain with a lazy running maximum m: m is
 //    raised only when a row's maximum exceeds it by more than 2^4, so O is
 //    rescaled rarely.  P = 2^(x - m + 4) <= 2^8 stays inside E4M3, and the
 //    +4 lifts the weights that matter out of E4M3's subnormal range (below
 //    2^-6), where a split term would lose its relative precision.
-//  * P enters the FP8 PV product as two E4M3 terms, P_hi = E4M3(P) and
-//    P_lo = E4M3(P - P_hi), each multiplied by V into the same TMEM
-//    accumulator.  One E4M3 term alone carries ~2 % relative error per
-//    weight, which shows in the output after its own E4M3 rounding; the
-//    pair carries ~2^-8.
+//  * P enters the FP8 PV product as two E4M3 terms, P_hi (P truncated to
+//    E4M3 precision) and P_lo = E4M3(P - P_hi), each multiplied by V into the
+//    same TMEM accumulator.  One E4M3 term alone carries ~2 % relative error
+//    per weight, which shows in the output after its own E4M3 rounding; the
+//    pair carries ~2^-7.
+#include <cuda.h>  // CUtensorMap and the cuTensorMapEncodeTiled prototype (resolved at run time)
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -87,27 +94,31 @@ __global__ void dequant_pages_kernel(const uint8_t* __restrict__ fp4, const uint
 // ---------------------------------------------------------------------------
 constexpr int kQB = 64;                    // queries per work unit
 constexpr int kQT = 32;                    // queries per M=128 tile (x 4 heads)
-constexpr int kKT = 128;                   // keys per KV tile (two pages)
-constexpr int kNP = 3;                     // packed-page ring stages
+constexpr int kKT = 64;                    // keys per KV tile (one page)
+constexpr int kNK = 4;                     // E4M3 K/V tile slots
+constexpr int kNP = 6;                     // packed-page ring stages
 constexpr int kCtxThreads = 512;
-constexpr int kTile = 128 * 128;           // one 128 x 128 E4M3 tile: 16 KB
+constexpr int kQTile = 128 * 128;          // one M-tile of Q, E4M3: 16 KB
+constexpr int kKVTile = kKT * 128;         // one K or V tile, E4M3: 8 KB
 constexpr int kPackedPage = kPage * kD / 2;   // 4 KB of codes per (page, KV head)
 constexpr int kScalePage = kPage * kD / 16;   // 512 B of scales per (page, KV head)
 constexpr float kRescaleLog2 = 4.f;        // lazy-maximum threshold
 constexpr float kPBiasLog2 = 4.f;          // P = 2^(x - m + 4): P <= 2^(4 + 4) = 256 < 448
 constexpr uint32_t kTmemCols = 512;
+// TMEM columns of M-tile T: S buffers at T*256 + {0, 64}, O at T*256 + 128.
+constexpr uint32_t kTmemPerTile = 256;
+constexpr uint32_t kTmemO = 128;
 
 struct CtxSmem {
-  uint8_t q[2][kTile];   // M-tiles 0/1 of Q       (128B-swizzled, K-major)
-  uint8_t k[2][kTile];   // E4M3 K, two slots      (128B-swizzled, K-major B operand)
-  uint8_t v[2][kTile];   // E4M3 V, two slots      (128B-swizzled, MN-major B operand)
-  uint8_t p[2][kTile];   // E4M3 P_hi of M-tiles 0/1 (128B-swizzled, K-major A operand)
-  uint8_t pl[2][kTile];  // E4M3 P_lo = E4M3(P - P_hi) of M-tiles 0/1
-  uint8_t pk[kNP][2][2][kPackedPage];  // [stage][K=0,V=1][page of the tile][slot*64 + byte]
-  uint8_t sf[kNP][2][2][kScalePage];   // [stage][K,V][page][slot*8 + block]
+  uint8_t q[2][kQTile];        // M-tiles 0/1 of Q (128B-swizzled, K-major A operand)
+  uint8_t k[kNK][kKVTile];     // E4M3 K tiles (128B-swizzled, K-major B operand of S = Q K^T)
+  uint8_t v[kNK][kKVTile];     // E4M3 V tiles (128B-swizzled, MN-major B operand of O += P V)
+  uint8_t pk[kNP][2][kPackedPage];  // [stage][K=0,V=1][slot*64 + byte]
+  uint8_t sf[kNP][2][kScalePage];   // [stage][K,V][slot*8 + block]
   uint64_t pk_full[kNP], pk_empty[kNP];
-  uint64_t k_ready[2], v_ready[2], kv_free[2];
-  uint64_t s_full[2], p_full[2];
+  uint64_t k_ready[kNK], v_ready[kNK], kv_free[kNK];
+  uint64_t s_full[2][2], p_full[2][2];  // [M-tile][S buffer]
+  uint64_t o_done[2];                   // PV of an M-tile completed (one phase per KV tile)
   uint64_t o_final, q_ready;
   uint32_t tmem_base;
   int unit_b, unit_qb;
@@ -157,25 +168,69 @@ __device__ void find_unit(const int32_t* __restrict__ qo, int B, int t, int& out
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// 2^x on two f16 values at once.
+__device__ __forceinline__ uint32_t ex2_h2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t hadd2_u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Two E4M3 bytes (low 16 bits, first element low) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)v));
+  return d;
+}
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 3-D tiled TMA load global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // Two floats -> two E4M3 bytes (x in the low byte), RNE, satfinite.
 __device__ __forceinline__ uint32_t f2_to_e4m3x2(float lo, float hi) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
-// (p0, p1) -> hi = E4M3(p) and lo = E4M3(p - hi), two bytes each (p0 low).
-// p is first rounded to f16 (11 significant bits); hi and lo are taken from
-// that value, and the difference f16(p) - hi is exact in f16 (hi lies within
-// a factor 1 +- 2^-4 of it, or both sit on the 2^-9 subnormal grid).
-__device__ __forceinline__ void split_e4m3x2(float p0, float p1, uint32_t& hi, uint32_t& lo) {
-  const __half2 ph = __floats2half2_rn(p0, p1);
-  hi = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&ph));
-  const __half2_raw hb = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)hi, __NV_E4M3);
-  const __half2 d = __hsub2(ph, *reinterpret_cast<const __half2*>(&hb));
-  lo = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&d));
+// ph = (p0, p1) as f16x2 -> hi = E4M3(p) and lo = E4M3(p - hi), two bytes
+// each (p0 low).  ph - hi is exact in f16: hi lies within a factor 1 +- 2^-4
+// of ph, or both sit on the 2^-9 grid of E4M3's subnormal range.
+__device__ __forceinline__ void split_e4m3x2(uint32_t ph, uint32_t& hi, uint32_t& lo) {
+  hi = f16x2_to_e4m3x2(ph);
+  lo = f16x2_to_e4m3x2(hsub2_u(ph, e4m3x2_to_f16x2(hi)));
 }
 
 __global__ void __launch_bounds__(kCtxThreads, 1)
-    ctx_nvfp4_kernel(const CtxArgs a, const float scale_log2, const float inv_out_scale) {
+    ctx_nvfp4_kernel(const CtxArgs a, const __grid_constant__ CUtensorMap q_map, const float scale_log2,
+                     const float inv_out_scale) {
   extern __shared__ uint8_t smem_raw[];
   CtxSmem& sm = *reinterpret_cast<CtxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -195,15 +250,20 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       mbar_init(smem_u32(&sm.pk_full[i]), 1);
       mbar_init(smem_u32(&sm.pk_empty[i]), 4);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNK; ++i) {
       mbar_init(smem_u32(&sm.k_ready[i]), 4);
       mbar_init(smem_u32(&sm.v_ready[i]), 4);
       mbar_init(smem_u32(&sm.kv_free[i]), 1);
-      mbar_init(smem_u32(&sm.s_full[i]), 1);
-      mbar_init(smem_u32(&sm.p_full[i]), 4);
+    }
+    for (int t = 0; t < 2; ++t) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(smem_u32(&sm.s_full[t][i]), 1);
+        mbar_init(smem_u32(&sm.p_full[t][i]), 4);
+      }
+      mbar_init(smem_u32(&sm.o_done[t]), 1);
     }
     mbar_init(smem_u32(&sm.o_final), 1);
-    mbar_init(smem_u32(&sm.q_ready), 2);
+    mbar_init(smem_u32(&sm.q_ready), 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -231,104 +291,100 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // One page per KV tile: packed K and V codes (4 KB each) and their scales
+    // (512 B each) through the block table.
     if (lane == 0 && n_tiles > 0) {
       const uint64_t pol = policy_evict_last();  // pages are re-read by the other query blocks
-      const int n_pages = (kv_len + kPage - 1) / kPage;
       for (int j = 0; j < n_tiles; ++j) {
         const int st = j % kNP;
         if (j >= kNP && !mbar_wait(smem_u32(&sm.pk_empty[st]), ((j / kNP) - 1) & 1, &g_ctx_err)) break;
-        const int np = min(2, n_pages - 2 * j);
-        const uint32_t fb = smem_u32(&sm.pk_full[st]);
-        mbar_arrive_expect_tx(fb, (uint32_t)np * 2u * (kPackedPage + kScalePage));
-        for (int h = 0; h < np; ++h) {
-          int phys = a.block_table[(int64_t)b * a.max_pages_per_seq + 2 * j + h];
-          if (phys < 0 || phys >= a.num_pages) {
-            atomicOr(&g_ctx_err, kErrBadIndex);
-            phys = 0;
-          }
-          const int64_t row = ((int64_t)phys * kHkv + g) * kPage;
-          bulk_g2s_hint(smem_u32(sm.pk[st][0][h]), a.k_fp4 + row * (kD / 2), kPackedPage, fb, pol);
-          bulk_g2s_hint(smem_u32(sm.sf[st][0][h]), a.k_sf + row * (kD / 16), kScalePage, fb, pol);
-          bulk_g2s_hint(smem_u32(sm.pk[st][1][h]), a.v_fp4 + row * (kD / 2), kPackedPage, fb, pol);
-          bulk_g2s_hint(smem_u32(sm.sf[st][1][h]), a.v_sf + row * (kD / 16), kScalePage, fb, pol);
+        int phys = a.block_table[(int64_t)b * a.max_pages_per_seq + j];
+        if (phys < 0 || phys >= a.num_pages) {
+          atomicOr(&g_ctx_err, kErrBadIndex);
+          phys = 0;
         }
+        const int64_t row = ((int64_t)phys * kHkv + g) * kPage;
+        const uint32_t fb = smem_u32(&sm.pk_full[st]);
+        mbar_arrive_expect_tx(fb, 2u * (kPackedPage + kScalePage));
+        bulk_g2s_hint(smem_u32(sm.pk[st][0]), a.k_fp4 + row * (kD / 2), kPackedPage, fb, pol);
+        bulk_g2s_hint(smem_u32(sm.sf[st][0]), a.k_sf + row * (kD / 16), kScalePage, fb, pol);
+        bulk_g2s_hint(smem_u32(sm.pk[st][1]), a.v_fp4 + row * (kD / 2), kPackedPage, fb, pol);
+        bulk_g2s_hint(smem_u32(sm.sf[st][1]), a.v_sf + row * (kD / 16), kScalePage, fb, pol);
       }
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
+    // S_T(j) goes to TMEM buffer j & 1 of M-tile T, so S of tile j+2 is
+    // computed while the softmax works on tile j+1.  P_T(j) is written by the
+    // softmax over the consumed S_T(j) columns (hi and lo, 8 columns each per
+    // 32 keys) and read from there as the A operand of PV.  Issue order per
+    // tile j: PV_0(j), S_0(j+2), PV_1(j), S_1(j+2); a commit after S_T(j+2)
+    // therefore also covers PV_T(j).
     if (lane == 0 && n_tiles > 0) {
-      constexpr uint32_t idS = tc::idesc_e4m3_f32(128, 128, false);  // B = K tile, K-major
+      constexpr uint32_t idS = tc::idesc_e4m3_f32(128, kKT, false);  // B = K tile, K-major
       constexpr uint32_t idO = tc::idesc_e4m3_f32(128, 128, true);   // B = V tile, MN-major
       const uint32_t q_base = smem_u32(sm.q[0]);
       const uint32_t k_base = smem_u32(sm.k[0]);
       const uint32_t v_base = smem_u32(sm.v[0]);
-      const uint32_t p_base = smem_u32(sm.p[0]);
-      auto issue_s = [&](int T, int slot) {
-        const uint32_t qa = q_base + (uint32_t)T * kTile;
-        const uint32_t ka = k_base + (uint32_t)slot * kTile;
+      auto issue_s = [&](int T, int j) {
+        const uint32_t qa = q_base + (uint32_t)T * kQTile;
+        const uint32_t ka = k_base + (uint32_t)(j % kNK) * kKVTile;
+        const uint32_t d = tmem + (uint32_t)T * kTmemPerTile + (uint32_t)(j & 1) * kKT;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          tc::mma_e4m3(tmem + T * 128, tc::sw128_desc(qa + 32 * k), tc::sw128_desc(ka + 32 * k), idS, k > 0);
+          tc::mma_e4m3(d, tc::sw128_desc(qa + 32 * k), tc::sw128_desc(ka + 32 * k), idS, k > 0);
+        tc::commit(smem_u32(&sm.s_full[T][j & 1]));
       };
-      const uint32_t pl_base = smem_u32(sm.pl[0]);
-      auto issue_pv = [&](int T, int slot, bool acc) {
-        const uint32_t pa = p_base + (uint32_t)T * kTile;
-        const uint32_t pla = pl_base + (uint32_t)T * kTile;
-        const uint32_t va = v_base + (uint32_t)slot * kTile;
+      auto issue_pv = [&](int T, int j) {
+        const uint32_t pa = tmem + (uint32_t)T * kTmemPerTile + (uint32_t)(j & 1) * kKT;
+        const uint32_t va = v_base + (uint32_t)(j % kNK) * kKVTile;
+        const uint32_t d = tmem + (uint32_t)T * kTmemPerTile + kTmemO;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          tc::mma_e4m3(tmem + 256 + T * 128, tc::sw128_desc(pa + 32 * k), tc::sw128_desc(va + 4096 * k), idO,
-                       (acc || k > 0) ? 1u : 0u);
-          tc::mma_e4m3(tmem + 256 + T * 128, tc::sw128_desc(pla + 32 * k), tc::sw128_desc(va + 4096 * k), idO, 1u);
+        for (int k = 0; k < kKT / 32; ++k) {
+          tc::mma_e4m3_tmem_a(d, pa + 16 * k, tc::sw128_desc(va + 4096 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
+          tc::mma_e4m3_tmem_a(d, pa + 16 * k + 8, tc::sw128_desc(va + 4096 * k), idO, 1u);
         }
+        tc::commit(smem_u32(&sm.o_done[T]));
       };
-      bool ok = mbar_wait(smem_u32(&sm.q_ready), 0, &g_ctx_err) &&
-                mbar_wait(smem_u32(&sm.k_ready[0]), 0, &g_ctx_err);
-      if (ok) {
+      bool ok = mbar_wait(smem_u32(&sm.q_ready), 0, &g_ctx_err);
+      for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
+        ok = mbar_wait(smem_u32(&sm.k_ready[j % kNK]), (j / kNK) & 1, &g_ctx_err);
+        if (!ok) break;
         tc::fence_after_thread_sync();
-        issue_s(0, 0);
-        tc::commit(smem_u32(&sm.s_full[0]));
-        issue_s(1, 0);
-        tc::commit(smem_u32(&sm.s_full[1]));
+        issue_s(0, j);
+        issue_s(1, j);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int slot = j & 1;
-        for (int T = 0; T < 2 && ok; ++T) {
-          ok = mbar_wait(smem_u32(&sm.p_full[T]), j & 1, &g_ctx_err);
-          if (ok && T == 0) ok = mbar_wait(smem_u32(&sm.v_ready[slot]), (j >> 1) & 1, &g_ctx_err);
+        for (int T = 0; T < 2; ++T) {
+          ok = mbar_wait(smem_u32(&sm.p_full[T][j & 1]), (j >> 1) & 1, &g_ctx_err);
+          if (ok && T == 0) ok = mbar_wait(smem_u32(&sm.v_ready[j % kNK]), (j / kNK) & 1, &g_ctx_err);
           if (!ok) break;
           tc::fence_after_thread_sync();
-          issue_pv(T, slot, j > 0);
-          if (T == 1) tc::commit(smem_u32(&sm.kv_free[slot]));
-          if (j + 1 < n_tiles) {
+          issue_pv(T, j);
+          if (T == 1) tc::commit(smem_u32(&sm.kv_free[j % kNK]));
+          if (j + 2 < n_tiles) {
             if (T == 0) {
-              ok = mbar_wait(smem_u32(&sm.k_ready[(j + 1) & 1]), ((j + 1) >> 1) & 1, &g_ctx_err);
+              ok = mbar_wait(smem_u32(&sm.k_ready[(j + 2) % kNK]), ((j + 2) / kNK) & 1, &g_ctx_err);
               if (!ok) break;
               tc::fence_after_thread_sync();
             }
-            issue_s(T, (j + 1) & 1);
-            tc::commit(smem_u32(&sm.s_full[T]));
+            issue_s(T, j + 2);
           }
         }
       }
       tc::commit(smem_u32(&sm.o_final));
     }
   } else if (warp < 4) {
-    // ----------------------------------------------------------- Q loaders
-    const int lt = threadIdx.x - 64;
-    for (int i = lt; i < 2 * 128 * 8; i += 64) {
-      const int T = i >> 10;
-      const int r = (i >> 3) & 127;
-      const int c = i & 7;
-      const int qrow = q0 + T * kQT + (r >> 2);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (qrow < q_len)
-        v = *reinterpret_cast<const uint4*>(a.q + ((int64_t)(qo + qrow) * kHq + g * kGroup + (r & 3)) * kD + c * 16);
-      *reinterpret_cast<uint4*>(sm.q[T] + swz(r, c)) = v;
+    // ------------------------------------------------------------ Q loader
+    // One TMA box per M-tile: [32 queries][4 heads][128 d] = rows r = 4*query
+    // + head, 128-byte swizzled by the tensor map.  Rows past total_q read as
+    // zero; rows of the next sequence are computed but never stored.
+    if (warp == 2 && lane == 0 && n_tiles > 0) {
+      const uint32_t qb_ = smem_u32(&sm.q_ready);
+      mbar_arrive_expect_tx(qb_, 2u * kQTile);
+      tma_load_3d(smem_u32(sm.q[0]), &q_map, 0, g * kGroup, qo + q0, qb_);
+      tma_load_3d(smem_u32(sm.q[1]), &q_map, 0, g * kGroup, qo + q0 + kQT, qb_);
     }
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&sm.q_ready));
   } else if (warp < 12) {
     // -------------------------------------------------------------- softmax
     const int T = (warp - 4) >> 2;
@@ -339,41 +395,66 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     int lim = kv_len - q_len + qrow;  // last visible key (inclusive)
     if (lim > kv_len - 1) lim = kv_len - 1;
     const uint32_t lane_off = (uint32_t)(32 * sub) << 16;
-    const uint32_t tS = tmem + lane_off + (uint32_t)(T * 128);
-    const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(T * 128);
-    uint8_t* prow = sm.p[T];
-    uint8_t* plrow = sm.pl[T];
+    const uint32_t tT = tmem + lane_off + (uint32_t)T * kTmemPerTile;
+    const uint32_t tO = tT + kTmemO;
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
+    const bool neg_scale = scale_log2 < 0.f;
     for (int j = 0; j < n_tiles; ++j) {
       // warp-uniform outcome: the TMEM accesses below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[T]), j & 1, &g_ctx_err))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[T][j & 1]), (j >> 1) & 1, &g_ctx_err))) {
         ok = false;
         break;
       }
       tc::fence_after_thread_sync();
+      const uint32_t tS = tT + (uint32_t)(j & 1) * kKT;
       const int kbase = j * kKT;
       const bool masked = kbase + kKT - 1 > lim;
-      // pass 1: row maximum of the scaled logits
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tc::ld32(tS + 32 * c, v);
+      // pass 1: extreme raw logit of the row (max, or min for a negative
+      // scale), then the scaled maximum in the exp2 domain
+      float ext = neg_scale ? INFINITY : -INFINITY;
+      {
+        uint32_t v0[32], v1[32];
+        tc::ld32(tS, v0);
+        tc::ld32(tS + 32, v1);
         tc::ld_wait();
+        if (!masked) {
+          float e0 = ext, e1 = u2f(v0[0]), e2 = u2f(v1[0]), e3 = u2f(v1[1]);
+          if (!neg_scale) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float x = u2f(v[i]) * scale_log2;
-          if (masked && kbase + 32 * c + i > lim) x = -INFINITY;
-          mx = fmaxf(mx, x);
+            for (int i = 1; i < 31; i += 2) {
+              e0 = max3(e0, u2f(v0[i]), u2f(v0[i + 1]));
+              e1 = max3(e1, u2f(v1[i + 1]), u2f(v1[i + 2]));
+            }
+            ext = max3(max3(e0, e1, e2), e3, u2f(v0[31]));
+          } else {
+#pragma unroll
+            for (int i = 1; i < 31; i += 2) {
+              e0 = min3(e0, u2f(v0[i]), u2f(v0[i + 1]));
+              e1 = min3(e1, u2f(v1[i + 1]), u2f(v1[i + 2]));
+            }
+            ext = min3(min3(e0, e1, e2), e3, u2f(v0[31]));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (kbase + i <= lim) ext = neg_scale ? fminf(ext, u2f(v0[i])) : fmaxf(ext, u2f(v0[i]));
+            if (kbase + 32 + i <= lim) ext = neg_scale ? fminf(ext, u2f(v1[i])) : fmaxf(ext, u2f(v1[i]));
+          }
         }
       }
+      const float mx = (ext == INFINITY || ext == -INFINITY) ? -INFINITY : ext * scale_log2;
       const float m_new = fmaxf(m_used, mx);
       const bool raise = m_new > m_used + kRescaleLog2;  // also true for the first finite maximum
       const float alpha = raise ? exp2f(m_used - m_new) : 1.f;  // 0 when m_used was -inf
       if (__any_sync(0xffffffffu, raise && j > 0)) {
-        // O_T holds PV of tiles < j (complete: this S_T(j) was committed after them)
+        // O_T must hold PV of every tile < j before it is rescaled
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_done[T]), (j - 1) & 1, &g_ctx_err))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_thread_sync();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -389,44 +470,51 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         l *= alpha;
         m_used = m_new;
       }
-      const bool dead = (m_used == -INFINITY);  // no visible key yet
-      const float m_off = m_used - kPBiasLog2;
-      // pass 2: P = 2^(x - m_used) as two E4M3 terms into the swizzled P tiles
-      float lsum = 0.f;
+      // pass 2: P = 2^(x - m_used + 4) (f32 ex2), split into E4M3 hi + lo and
+      // stored over the consumed S columns: keys 32c..32c+31 -> hi at columns
+      // 16c..16c+7, lo at 16c+8..16c+15 (4 keys per column).  hi is P
+      // truncated to E4M3's 3 mantissa bits (a mask of the f32 bits), lo =
+      // P - hi is exact in f32; hi + lo carries P to ~2^-7.  Masked keys (and
+      // every key of a row that has seen none) become 2^-inf = 0.
+      const float2 cc = make_float2(scale_log2, scale_log2);
+      const float2 mm = make_float2(kPBiasLog2 - m_used, kPBiasLog2 - m_used);
+      float2 lacc = make_float2(0.f, 0.f);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kKT / 32; ++c) {
         uint32_t v[32];
         tc::ld32(tS + 32 * c, v);
         tc::ld_wait();
-        uint32_t ph[8], pl[8];
+        uint32_t pp[16];  // [0..7] hi, [8..15] lo
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int k0 = kbase + 32 * c + 2 * i;
-          float p0 = fast_exp2(fmaf(u2f(v[2 * i]), scale_log2, -m_off));
-          float p1 = fast_exp2(fmaf(u2f(v[2 * i + 1]), scale_log2, -m_off));
-          if (dead || (masked && k0 > lim)) p0 = 0.f;
-          if (dead || (masked && k0 + 1 > lim)) p1 = 0.f;
-          lsum += p0 + p1;
-          uint32_t hi, lo;
-          split_e4m3x2(p0, p1, hi, lo);
+          float2 x = __ffma2_rn(make_float2(u2f(v[2 * i]), u2f(v[2 * i + 1])), cc, mm);
+          if (masked) {
+            const int k0 = kbase + 32 * c + 2 * i;
+            if (k0 > lim) x.x = -INFINITY;
+            if (k0 + 1 > lim) x.y = -INFINITY;
+          }
+          const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          lacc = __fadd2_rn(lacc, p);
+          const float2 h = make_float2(__uint_as_float(__float_as_uint(p.x) & 0xFFF00000u),
+                                       __uint_as_float(__float_as_uint(p.y) & 0xFFF00000u));
+          const float2 lo = __ffma2_rn(h, make_float2(-1.f, -1.f), p);
+          const uint32_t hc = f2_to_e4m3x2(h.x, h.y);
+          const uint32_t lc = f2_to_e4m3x2(lo.x, lo.y);
           if (i & 1) {
-            ph[i >> 1] |= hi << 16;
-            pl[i >> 1] |= lo << 16;
+            pp[i >> 1] = __byte_perm(pp[i >> 1], hc, 0x5410);
+            pp[8 + (i >> 1)] = __byte_perm(pp[8 + (i >> 1)], lc, 0x5410);
           } else {
-            ph[i >> 1] = hi;
-            pl[i >> 1] = lo;
+            pp[i >> 1] = hc;
+            pp[8 + (i >> 1)] = lc;
           }
         }
-        *reinterpret_cast<uint4*>(prow + swz(r, 2 * c)) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        *reinterpret_cast<uint4*>(prow + swz(r, 2 * c + 1)) = make_uint4(ph[4], ph[5], ph[6], ph[7]);
-        *reinterpret_cast<uint4*>(plrow + swz(r, 2 * c)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-        *reinterpret_cast<uint4*>(plrow + swz(r, 2 * c + 1)) = make_uint4(pl[4], pl[5], pl[6], pl[7]);
+        tc::st16(tS + 16 * c, pp);
       }
-      l += lsum;
-      tc::fence_proxy_async_smem();
+      l += lacc.x + lacc.y;
+      tc::st_wait();
       tc::fence_before_thread_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[T]));
+      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[T][j & 1]));
     }
     // ------------------------------------------------------------ epilogue
     bool have_o = false;
@@ -461,26 +549,25 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- dequantisers
+    // Tile j (64 keys): K then V, 512 items of (key, 16-element block) each.
     const int dt = threadIdx.x - 384;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % kNP;
-      const int slot = j & 1;
+      const int slot = j % kNK;
       if (!mbar_wait(smem_u32(&sm.pk_full[st]), (j / kNP) & 1, &g_ctx_err)) break;
-      if (j >= 2 && !mbar_wait(smem_u32(&sm.kv_free[slot]), ((j >> 1) - 1) & 1, &g_ctx_err)) break;
+      if (j >= kNK && !mbar_wait(smem_u32(&sm.kv_free[slot]), ((j / kNK) - 1) & 1, &g_ctx_err)) break;
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
         uint8_t* dst = kv == 0 ? sm.k[slot] : sm.v[slot];
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
+        for (int it = 0; it < kKT * 8 / 128; ++it) {
           const int i = dt + 128 * it;  // item = (key, 16-element block)
           const int key = i >> 3;
           const int blk = i & 7;
           uint4 out = make_uint4(0u, 0u, 0u, 0u);
           if (j * kKT + key < kv_len) {
-            const int h = key >> 6;
-            const int s = key & 63;
-            const uint2 packed = *reinterpret_cast<const uint2*>(&sm.pk[st][kv][h][s * 64 + blk * 8]);
-            out = dequant16(packed, sm.sf[st][kv][h][s * 8 + blk]);
+            const uint2 packed = *reinterpret_cast<const uint2*>(&sm.pk[st][kv][key * 64 + blk * 8]);
+            out = dequant16(packed, sm.sf[st][kv][key * 8 + blk]);
           }
           *reinterpret_cast<uint4*>(dst + swz(key, blk)) = out;
         }
@@ -526,18 +613,51 @@ cudaError_t launch_dequant_pages(const uint8_t* fp4, const uint8_t* sf, const in
   return cudaGetLastError();
 }
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+// Tensor map over q [total_q][32 heads][128 d] (E4M3 bytes): boxes of
+// [32 tokens][4 heads][128 d], 128-byte swizzle, zero fill out of range.
+cudaError_t make_q_map(const uint8_t* q, int64_t total_q, CUtensorMap* map) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  if (!g_encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kHq, (cuuint64_t)total_q};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD, (cuuint64_t)kHq * kD};
+  const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)kGroup, (cuuint32_t)kQT};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(q), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+}  // namespace
+
 cudaError_t launch_ctx(const CtxArgs& a, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = ensure_ctx_smem(dev)) != cudaSuccess) return e;
+  alignas(64) CUtensorMap q_map;
+  if ((e = make_q_map(a.q, a.total_q, &q_map)) != cudaSuccess) return e;
   // Upper bound on the number of (sequence, 64-query block) units without
   // reading qo_indptr on the host: sum_b ceil(q_len_b / 64) <= total_q / 64 + batch.
   const int64_t blocks = (a.total_q + kQB - 1) / kQB + a.batch;
   const int64_t grid = blocks * kHkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const float scale_log2 = a.q_scale / sqrtf((float)kD) * 1.4426950408889634f;
-  ctx_nvfp4_kernel<<<(unsigned)grid, kCtxThreads, kCtxSmemBytes, stream>>>(a, scale_log2, 1.f / a.out_scale);
+  ctx_nvfp4_kernel<<<(unsigned)grid, kCtxThreads, kCtxSmemBytes, stream>>>(a, q_map, scale_log2,
+                                                                           1.f / a.out_scale);
   return cudaGetLastError();
 }
 

@@ -8,7 +8,9 @@
 // 2 significant bits and an E4M3 value at most 4, every product lies within
 // [2^-10, 2688] in magnitude (or is zero), and f16 holds 11 significant bits
 // over [2^-14, 65504].  The single rounding is the hardware's f16x2 -> e4m3x2
-// conversion (round to nearest even, saturating to +-448).
+// conversion (round to nearest even, saturating to +-448).  Conversions run
+// at a fraction of the ALU rate on sm_103a, so the per-element work below is
+// byte permutes through a per-block table.
 #pragma once
 #include <cstdint>
 
@@ -43,22 +45,33 @@ __device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
   return r;
 }
 
-// Four packed bytes (8 E2M1 codes, element order low nibble first) sharing
-// one scale (as f16x2 broadcast) -> 8 E4M3 bytes in element order.
-__device__ __forceinline__ uint2 dequant8(uint32_t packed, uint32_t scale_h2) {
-  const uint32_t a = f16x2_to_e4m3x2(hmul2_u32(e2m1x2_to_f16x2(packed), scale_h2));
-  const uint32_t b = f16x2_to_e4m3x2(hmul2_u32(e2m1x2_to_f16x2(packed >> 8), scale_h2));
-  const uint32_t c = f16x2_to_e4m3x2(hmul2_u32(e2m1x2_to_f16x2(packed >> 16), scale_h2));
-  const uint32_t d = f16x2_to_e4m3x2(hmul2_u32(e2m1x2_to_f16x2(packed >> 24), scale_h2));
-  return make_uint2(a | (b << 16), c | (d << 16));
+// One 16-element block: 8 packed bytes + its scale byte -> 16 E4M3 bytes.
+//
+// A block has one scale, so its 16 possible outputs are tabulated first: the
+// 8 E2M1 magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6} (f16x2 constants) times the
+// scale, rounded to E4M3 -- 4 products and 4 conversions per block instead of
+// 16 + 8.  Each group of 4 codes (16 bits, element order low nibble first)
+// then becomes 4 output bytes with two byte-permutes: the low 3 bits of each
+// nibble index the magnitude table, and bit 3 (the E2M1 sign) selects a
+// 0x80 byte that is XORed into the E4M3 sign.  Same values, bit for bit, as
+// converting every element: the products are exact in f16 and each is
+// rounded once, by the same conversion.
+__device__ __forceinline__ uint32_t nvfp4_lookup4(uint32_t codes16, uint32_t tab_lo, uint32_t tab_hi) {
+  const uint32_t mag = __byte_perm(tab_lo, tab_hi, codes16 & 0x7777u);
+  const uint32_t sgn = __byte_perm(0u, 0x80808080u, (codes16 >> 1) & 0x4444u);
+  return mag ^ sgn;
 }
 
-// One 16-element block: 8 packed bytes + its scale byte -> 16 E4M3 bytes.
 __device__ __forceinline__ uint4 dequant16(uint2 packed, uint32_t sf_byte) {
   const uint32_t s = e4m3_to_f16x2_bcast(sf_byte);
-  const uint2 lo = dequant8(packed.x, s);
-  const uint2 hi = dequant8(packed.y, s);
-  return make_uint4(lo.x, lo.y, hi.x, hi.y);
+  const uint32_t t01 = f16x2_to_e4m3x2(hmul2_u32(0x38000000u, s));  // (0, 0.5)
+  const uint32_t t23 = f16x2_to_e4m3x2(hmul2_u32(0x3E003C00u, s));  // (1, 1.5)
+  const uint32_t t45 = f16x2_to_e4m3x2(hmul2_u32(0x42004000u, s));  // (2, 3)
+  const uint32_t t67 = f16x2_to_e4m3x2(hmul2_u32(0x46004400u, s));  // (4, 6)
+  const uint32_t tab_lo = t01 | (t23 << 16);
+  const uint32_t tab_hi = t45 | (t67 << 16);
+  return make_uint4(nvfp4_lookup4(packed.x & 0xffffu, tab_lo, tab_hi), nvfp4_lookup4(packed.x >> 16, tab_lo, tab_hi),
+                    nvfp4_lookup4(packed.y & 0xffffu, tab_lo, tab_hi), nvfp4_lookup4(packed.y >> 16, tab_lo, tab_hi));
 }
 
 }  // namespace gqa
