@@ -120,6 +120,7 @@ struct CtxSmem {
   uint64_t s_full[2][2], p_full[2][2];  // [M-tile][S buffer]
   uint64_t o_done[2];                   // PV of an M-tile completed (one phase per KV tile)
   uint64_t o_final, q_ready;
+  uint2 sftab[256];      // E4M3 magnitudes of the 8 E2M1 codes for every scale byte
   uint32_t tmem_base;
   int unit_b, unit_qb;
 };
@@ -167,6 +168,19 @@ __device__ void find_unit(const int32_t* __restrict__ qo, int B, int t, int& out
 }
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// p with its f32 mantissa cut to E4M3's 3 bits (exact E4M3 value for
+// 2^-6 <= p <= 448; below that the conversion rounds further).
+__device__ __forceinline__ float trunc_e4m3(float p) { return __uint_as_float(__float_as_uint(p) & 0xFFF00000u); }
+
+// Four floats -> four E4M3 bytes (e0 in the low byte), rounding toward zero,
+// saturating.  The stochastic-rounding conversion with all random bits zero
+// truncates; one instruction packs all four bytes.
+__device__ __forceinline__ uint32_t e4m3x4_rz(float e0, float e1, float e2, float e3) {
+  uint32_t r;
+  asm("cvt.rs.satfinite.e4m3x4.f32 %0, {%1, %2, %3, %4}, %5;" : "=r"(r) : "f"(e3), "f"(e2), "f"(e1), "f"(e0), "r"(0u));
+  return r;
+}
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
@@ -245,6 +259,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       sm.unit_qb = uqb;
     }
   }
+  for (int i = threadIdx.x; i < 256; i += kCtxThreads) sm.sftab[i] = nvfp4_scale_table((uint32_t)i);
   if (threadIdx.x == 32) {
     for (int i = 0; i < kNP; ++i) {
       mbar_init(smem_u32(&sm.pk_full[i]), 1);
@@ -320,59 +335,101 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     // 32 keys) and read from there as the A operand of PV.  Issue order per
     // tile j: PV_0(j), S_0(j+2), PV_1(j), S_1(j+2); a commit after S_T(j+2)
     // therefore also covers PV_T(j).
-    if (lane == 0 && n_tiles > 0) {
+    // The whole warp runs this loop (descriptor arithmetic stays warp-uniform,
+    // which keeps it in the uniform datapath the MMA reads); one elected lane
+    // issues each MMA and commit.  Descriptors are built once and advanced by
+    // adding the byte offset / 16 to their start-address field.
+    if (n_tiles > 0) {
       constexpr uint32_t idS = tc::idesc_e4m3_f32(128, kKT, false);  // B = K tile, K-major
       constexpr uint32_t idO = tc::idesc_e4m3_f32(128, 128, true);   // B = V tile, MN-major
-      const uint32_t q_base = smem_u32(sm.q[0]);
-      const uint32_t k_base = smem_u32(sm.k[0]);
-      const uint32_t v_base = smem_u32(sm.v[0]);
+      const uint64_t dq0 = tc::sw128_desc(smem_u32(sm.q[0]));
+      const uint64_t dk0 = tc::sw128_desc(smem_u32(sm.k[0]));
+      const uint64_t dv0 = tc::sw128_desc(smem_u32(sm.v[0]));
+      const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
       auto issue_s = [&](int T, int j) {
-        const uint32_t qa = q_base + (uint32_t)T * kQTile;
-        const uint32_t ka = k_base + (uint32_t)(j % kNK) * kKVTile;
-        const uint32_t d = tmem + (uint32_t)T * kTmemPerTile + (uint32_t)(j & 1) * kKT;
+        const uint64_t dq = dq0 + (uint64_t)(T * (kQTile >> 4));
+        const uint64_t dk = dk0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
+        const uint32_t d = tm + (uint32_t)T * kTmemPerTile + (uint32_t)(j & 1) * kKT;
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_e4m3(d, tc::sw128_desc(qa + 32 * k), tc::sw128_desc(ka + 32 * k), idS, k > 0);
-        tc::commit(smem_u32(&sm.s_full[T][j & 1]));
-      };
-      auto issue_pv = [&](int T, int j) {
-        const uint32_t pa = tmem + (uint32_t)T * kTmemPerTile + (uint32_t)(j & 1) * kKT;
-        const uint32_t va = v_base + (uint32_t)(j % kNK) * kKVTile;
-        const uint32_t d = tmem + (uint32_t)T * kTmemPerTile + kTmemO;
-#pragma unroll
-        for (int k = 0; k < kKT / 32; ++k) {
-          tc::mma_e4m3_tmem_a(d, pa + 16 * k, tc::sw128_desc(va + 4096 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
-          tc::mma_e4m3_tmem_a(d, pa + 16 * k + 8, tc::sw128_desc(va + 4096 * k), idO, 1u);
+          for (int k = 0; k < 4; ++k) tc::mma_e4m3(d, dq + 2 * k, dk + 2 * k, idS, k > 0);
+          tc::commit(smem_u32(&sm.s_full[T][j & 1]));
         }
-        tc::commit(smem_u32(&sm.o_done[T]));
+        __syncwarp();
       };
-      bool ok = mbar_wait(smem_u32(&sm.q_ready), 0, &g_ctx_err);
+      auto issue_pv = [&](int T, int j, bool free_kv) {
+        const uint32_t pa = tm + (uint32_t)T * kTmemPerTile + (uint32_t)(j & 1) * kKT;
+        const uint64_t dv = dv0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
+        const uint32_t d = tm + (uint32_t)T * kTmemPerTile + kTmemO;
+        if (tc::elect_one()) {
+#pragma unroll
+          for (int k = 0; k < kKT / 32; ++k) {
+            tc::mma_e4m3_tmem_a(d, pa + 16 * k, dv + 256 * k, idO, (j > 0 || k > 0) ? 1u : 0u);
+            tc::mma_e4m3_tmem_a(d, pa + 16 * k + 8, dv + 256 * k, idO, 1u);
+          }
+          tc::commit(smem_u32(&sm.o_done[T]));
+          if (free_kv) tc::commit(smem_u32(&sm.kv_free[j % kNK]));
+        }
+        __syncwarp();
+      };
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, &g_ctx_err));
+      };
+      bool ok = wait_all(&sm.q_ready, 0);
       for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
-        ok = mbar_wait(smem_u32(&sm.k_ready[j % kNK]), (j / kNK) & 1, &g_ctx_err);
+        ok = wait_all(&sm.k_ready[j % kNK], (j / kNK) & 1);
         if (!ok) break;
         tc::fence_after_thread_sync();
         issue_s(0, j);
         issue_s(1, j);
       }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        for (int T = 0; T < 2; ++T) {
-          ok = mbar_wait(smem_u32(&sm.p_full[T][j & 1]), (j >> 1) & 1, &g_ctx_err);
-          if (ok && T == 0) ok = mbar_wait(smem_u32(&sm.v_ready[j % kNK]), (j / kNK) & 1, &g_ctx_err);
-          if (!ok) break;
-          tc::fence_after_thread_sync();
-          issue_pv(T, j);
-          if (T == 1) tc::commit(smem_u32(&sm.kv_free[j % kNK]));
-          if (j + 2 < n_tiles) {
-            if (T == 0) {
-              ok = mbar_wait(smem_u32(&sm.k_ready[(j + 2) % kNK]), ((j + 2) / kNK) & 1, &g_ctx_err);
-              if (!ok) break;
-              tc::fence_after_thread_sync();
-            }
-            issue_s(T, j + 2);
+      // Event loop: never block on one M-tile while the other could proceed.
+      // PV_T(j) needs P_T(j) and V_j; S_T(j) needs K_j and PV_T(j-2) issued
+      // (it reuses that S buffer).  KV tile j is released after the second
+      // of its two PVs (a commit covers every MMA issued before it).
+      int nj[2] = {0, 0};                                           // next PV tile
+      int ns[2] = {n_tiles < 2 ? n_tiles : 2, n_tiles < 2 ? n_tiles : 2};  // next S tile
+      int turn = 0;
+      uint64_t t_idle = 0;
+      auto ready = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_try_wait(smem_u32(bar), parity));
+      };
+      while (ok && (nj[0] < n_tiles || nj[1] < n_tiles)) {
+        bool progressed = false;
+#pragma unroll
+        for (int probe = 0; probe < 2; ++probe) {
+          const int c = turn ^ probe;
+          const int j = nj[c];
+          if (j < n_tiles && j < ns[c] && ready(&sm.p_full[c][j & 1], (j >> 1) & 1) &&
+              ready(&sm.v_ready[j % kNK], (j / kNK) & 1)) {
+            tc::fence_after_thread_sync();
+            issue_pv(c, j, nj[c ^ 1] > j);
+            nj[c] = j + 1;
+            progressed = true;
+          }
+          const int js = ns[c];
+          if (js < n_tiles && js < nj[c] + 2 && ready(&sm.k_ready[js % kNK], (js / kNK) & 1)) {
+            tc::fence_after_thread_sync();
+            issue_s(c, js);
+            ns[c] = js + 1;
+            progressed = true;
           }
         }
+        turn ^= 1;
+        if (progressed) {
+          t_idle = 0;
+        } else {
+          const uint64_t now = global_timer_ns();
+          if (t_idle == 0) t_idle = now;
+          if (now - t_idle > kWaitNs) {
+            if (lane == 0) atomicOr(&g_ctx_err, kErrWaitTimeout);
+            ok = false;
+          }
+          __nanosleep(32);
+        }
       }
-      tc::commit(smem_u32(&sm.o_final));
+      if (tc::elect_one()) tc::commit(smem_u32(&sm.o_final));
+      __syncwarp();
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ Q loader
@@ -473,9 +530,10 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       // pass 2: P = 2^(x - m_used + 4) (f32 ex2), split into E4M3 hi + lo and
       // stored over the consumed S columns: keys 32c..32c+31 -> hi at columns
       // 16c..16c+7, lo at 16c+8..16c+15 (4 keys per column).  hi is P
-      // truncated to E4M3's 3 mantissa bits (a mask of the f32 bits), lo =
-      // P - hi is exact in f32; hi + lo carries P to ~2^-7.  Masked keys (and
-      // every key of a row that has seen none) become 2^-inf = 0.
+      // truncated to E4M3's 3 mantissa bits, lo = P - hi (exact in f32) is
+      // itself truncated to E4M3: hi + lo carries P to within 2^-7 of its
+      // value, always from below.  Masked keys (and every key of a row that
+      // has seen none) become 2^-inf = 0.
       const float2 cc = make_float2(scale_log2, scale_log2);
       const float2 mm = make_float2(kPBiasLog2 - m_used, kPBiasLog2 - m_used);
       float2 lacc = make_float2(0.f, 0.f);
@@ -486,27 +544,26 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         tc::ld_wait();
         uint32_t pp[16];  // [0..7] hi, [8..15] lo
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float2 x = __ffma2_rn(make_float2(u2f(v[2 * i]), u2f(v[2 * i + 1])), cc, mm);
+        for (int q = 0; q < 8; ++q) {  // keys 4q .. 4q+3 of the chunk
+          float2 x01 = __ffma2_rn(make_float2(u2f(v[4 * q]), u2f(v[4 * q + 1])), cc, mm);
+          float2 x23 = __ffma2_rn(make_float2(u2f(v[4 * q + 2]), u2f(v[4 * q + 3])), cc, mm);
           if (masked) {
-            const int k0 = kbase + 32 * c + 2 * i;
-            if (k0 > lim) x.x = -INFINITY;
-            if (k0 + 1 > lim) x.y = -INFINITY;
+            const int k0 = kbase + 32 * c + 4 * q;
+            if (k0 > lim) x01.x = -INFINITY;
+            if (k0 + 1 > lim) x01.y = -INFINITY;
+            if (k0 + 2 > lim) x23.x = -INFINITY;
+            if (k0 + 3 > lim) x23.y = -INFINITY;
           }
-          const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          lacc = __fadd2_rn(lacc, p);
-          const float2 h = make_float2(__uint_as_float(__float_as_uint(p.x) & 0xFFF00000u),
-                                       __uint_as_float(__float_as_uint(p.y) & 0xFFF00000u));
-          const float2 lo = __ffma2_rn(h, make_float2(-1.f, -1.f), p);
-          const uint32_t hc = f2_to_e4m3x2(h.x, h.y);
-          const uint32_t lc = f2_to_e4m3x2(lo.x, lo.y);
-          if (i & 1) {
-            pp[i >> 1] = __byte_perm(pp[i >> 1], hc, 0x5410);
-            pp[8 + (i >> 1)] = __byte_perm(pp[8 + (i >> 1)], lc, 0x5410);
-          } else {
-            pp[i >> 1] = hc;
-            pp[8 + (i >> 1)] = lc;
-          }
+          const float2 p01 = make_float2(fast_exp2(x01.x), fast_exp2(x01.y));
+          const float2 p23 = make_float2(fast_exp2(x23.x), fast_exp2(x23.y));
+          lacc = __fadd2_rn(lacc, p01);
+          lacc = __fadd2_rn(lacc, p23);
+          const float2 h01 = make_float2(trunc_e4m3(p01.x), trunc_e4m3(p01.y));
+          const float2 h23 = make_float2(trunc_e4m3(p23.x), trunc_e4m3(p23.y));
+          const float2 l01 = __ffma2_rn(h01, make_float2(-1.f, -1.f), p01);
+          const float2 l23 = __ffma2_rn(h23, make_float2(-1.f, -1.f), p23);
+          pp[q] = e4m3x4_rz(h01.x, h01.y, h23.x, h23.y);
+          pp[8 + q] = e4m3x4_rz(l01.x, l01.y, l23.x, l23.y);
         }
         tc::st16(tS + 16 * c, pp);
       }
@@ -567,7 +624,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
           uint4 out = make_uint4(0u, 0u, 0u, 0u);
           if (j * kKT + key < kv_len) {
             const uint2 packed = *reinterpret_cast<const uint2*>(&sm.pk[st][kv][key * 64 + blk * 8]);
-            out = dequant16(packed, sm.sf[st][kv][key * 8 + blk]);
+            out = dequant16_table(packed, sm.sftab[sm.sf[st][kv][key * 8 + blk]]);
           }
           *reinterpret_cast<uint4*>(dst + swz(key, blk)) = out;
         }

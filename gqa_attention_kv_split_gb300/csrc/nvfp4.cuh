@@ -62,16 +62,26 @@ __device__ __forceinline__ uint32_t nvfp4_lookup4(uint32_t codes16, uint32_t tab
   return mag ^ sgn;
 }
 
-__device__ __forceinline__ uint4 dequant16(uint2 packed, uint32_t sf_byte) {
+// The 8 E4M3 magnitudes of one scale: tab_lo = codes 0..3, tab_hi = codes
+// 4..7, one byte each (code c in byte c & 3).
+__device__ __forceinline__ uint2 nvfp4_scale_table(uint32_t sf_byte) {
   const uint32_t s = e4m3_to_f16x2_bcast(sf_byte);
   const uint32_t t01 = f16x2_to_e4m3x2(hmul2_u32(0x38000000u, s));  // (0, 0.5)
   const uint32_t t23 = f16x2_to_e4m3x2(hmul2_u32(0x3E003C00u, s));  // (1, 1.5)
   const uint32_t t45 = f16x2_to_e4m3x2(hmul2_u32(0x42004000u, s));  // (2, 3)
   const uint32_t t67 = f16x2_to_e4m3x2(hmul2_u32(0x46004400u, s));  // (4, 6)
-  const uint32_t tab_lo = t01 | (t23 << 16);
-  const uint32_t tab_hi = t45 | (t67 << 16);
-  return make_uint4(nvfp4_lookup4(packed.x & 0xffffu, tab_lo, tab_hi), nvfp4_lookup4(packed.x >> 16, tab_lo, tab_hi),
-                    nvfp4_lookup4(packed.y & 0xffffu, tab_lo, tab_hi), nvfp4_lookup4(packed.y >> 16, tab_lo, tab_hi));
+  return make_uint2(t01 | (t23 << 16), t45 | (t67 << 16));
+}
+
+// One 16-element block through a scale table: 8 packed bytes -> 16 E4M3 bytes.
+__device__ __forceinline__ uint4 dequant16_table(uint2 packed, uint2 tab) {
+  return make_uint4(nvfp4_lookup4(packed.x & 0xffffu, tab.x, tab.y), nvfp4_lookup4(packed.x >> 16, tab.x, tab.y),
+                    nvfp4_lookup4(packed.y & 0xffffu, tab.x, tab.y), nvfp4_lookup4(packed.y >> 16, tab.x, tab.y));
+}
+
+// One 16-element block: 8 packed bytes + its scale byte -> 16 E4M3 bytes.
+__device__ __forceinline__ uint4 dequant16(uint2 packed, uint32_t sf_byte) {
+  return dequant16_table(packed, nvfp4_scale_table(sf_byte));
 }
 
 }  // namespace gqa

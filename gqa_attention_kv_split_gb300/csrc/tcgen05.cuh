@@ -49,6 +49,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
   return d;
 }
 
+// One lane of the (converged) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Instruction descriptor, kind::f8f6f4, E4M3 x E4M3 -> F32, dense.
 //   bits 4-5 D format (1 = F32); 7-9 A format (0 = E4M3); 10-12 B format
 //   (0 = E4M3); 15 A major (0 = K); 16 B major (0 = K, 1 = MN);
