@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       int turn = 0;
       uint64_t t_idle = 0;
       auto ready = [&](uint64_t* bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_try_wait(smem_u32(bar), parity));
+        return __all_sync(0xffffffffu, mbar_test_wait(smem_u32(bar), parity));
       };
       while (ok && (nj[0] < n_tiles || nj[1] < n_tiles)) {
         bool progressed = false;
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
             if (lane == 0) atomicOr(&g_ctx_err, kErrWaitTimeout);
             ok = false;
           }
-          __nanosleep(32);
+          __nanosleep(128);
         }
       }
       if (tc::elect_one()) tc::commit(smem_u32(&sm.o_final));
@@ -471,11 +471,12 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       // pass 1: extreme raw logit of the row (max, or min for a negative
       // scale), then the scaled maximum in the exp2 domain
       float ext = neg_scale ? INFINITY : -INFINITY;
+      // the tile's 64 logits stay in registers for both passes
+      uint32_t v0[32], v1[32];
+      tc::ld32(tS, v0);
+      tc::ld32(tS + 32, v1);
+      tc::ld_wait();
       {
-        uint32_t v0[32], v1[32];
-        tc::ld32(tS, v0);
-        tc::ld32(tS + 32, v1);
-        tc::ld_wait();
         if (!masked) {
           float e0 = ext, e1 = u2f(v0[0]), e2 = u2f(v1[0]), e3 = u2f(v1[1]);
           if (!neg_scale) {
@@ -504,7 +505,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       const float mx = (ext == INFINITY || ext == -INFINITY) ? -INFINITY : ext * scale_log2;
       const float m_new = fmaxf(m_used, mx);
       const bool raise = m_new > m_used + kRescaleLog2;  // also true for the first finite maximum
-      const float alpha = raise ? exp2f(m_used - m_new) : 1.f;  // 0 when m_used was -inf
+      const float alpha = raise ? fast_exp2(m_used - m_new) : 1.f;  // 0 when m_used was -inf
       if (__any_sync(0xffffffffu, raise && j > 0)) {
         // O_T must hold PV of every tile < j before it is rescaled
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_done[T]), (j - 1) & 1, &g_ctx_err))) {
@@ -537,11 +538,9 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       const float2 cc = make_float2(scale_log2, scale_log2);
       const float2 mm = make_float2(kPBiasLog2 - m_used, kPBiasLog2 - m_used);
       float2 lacc = make_float2(0.f, 0.f);
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < kKT / 32; ++c) {
-        uint32_t v[32];
-        tc::ld32(tS + 32 * c, v);
-        tc::ld_wait();
+        const uint32_t* v = c == 0 ? v0 : v1;
         uint32_t pp[16];  // [0..7] hi, [8..15] lo
 #pragma unroll
         for (int q = 0; q < 8; ++q) {  // keys 4q .. 4q+3 of the chunk
