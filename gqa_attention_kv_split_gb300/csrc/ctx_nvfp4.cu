@@ -20,16 +20,16 @@
 //    j+1.  P is written back over the consumed S columns and read from TMEM
 //    as the A operand of PV.
 //  * Warp roles (16 warps): 0 = bulk-copy producer of packed NVFP4 pages +
-//    scales through the block table into a 6-stage ring; 1 = TMEM owner and
-//    single-thread tcgen05 MMA issuer; 2 = Q loader (two TMA boxes through a
-//    128-byte-swizzling tensor map); 3 = idle;
+//    scales through the block table into a 6-stage ring; 1 and 3 = tcgen05
+//    MMA issuers of M-tile 0 and 1 (warp 1 also owns the TMEM allocation);
+//    2 = Q loader (two TMA boxes through a 128-byte-swizzling tensor map);
 //    4-7 and 8-11 = softmax of M-tile 0 and 1 (one thread per TMEM lane =
 //    row); 12-15 = dequantisers writing E4M3 K and V tiles in the 128-byte
 //    swizzled layout the MMA descriptors read (K as the K-major B operand of
 //    S = Q K^T, V as the MN-major B operand of O = P V).
-//  * MMA order per KV tile j: PV_0(j), S_0(j+2), PV_1(j), S_1(j+2).  A
-//    softmax warp that raises its running maximum waits for the PV of the
-//    previous tile (o_done) before rescaling O in TMEM.
+//  * MMA order of M-tile T per KV tile j: PV_T(j), S_T(j+2).  A softmax warp
+//    that raises its running maximum waits for the PV of the previous tile
+//    (o_done) before rescaling O in TMEM.
 //  * Online softmax in the exp2 domain with a lazy running maximum m: m is
 //    raised only when a row's maximum exceeds it by more than 2^4, so O is
 //    rescaled rarely.  P = 2^(x - m + 4) <= 2^8 stays inside E4M3, and the
@@ -119,7 +119,7 @@ struct CtxSmem {
   uint64_t k_ready[kNK], v_ready[kNK], kv_free[kNK];
   uint64_t s_full[2][2], p_full[2][2];  // [M-tile][S buffer]
   uint64_t o_done[2];                   // PV of an M-tile completed (one phase per KV tile)
-  uint64_t o_final, q_ready;
+  uint64_t o_final[2], q_ready;  // o_final: every MMA of an M-tile completed
   uint2 sftab[256];      // E4M3 magnitudes of the 8 E2M1 codes for every scale byte
   uint32_t tmem_base;
   int unit_b, unit_qb;
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     for (int i = 0; i < kNK; ++i) {
       mbar_init(smem_u32(&sm.k_ready[i]), 4);
       mbar_init(smem_u32(&sm.v_ready[i]), 4);
-      mbar_init(smem_u32(&sm.kv_free[i]), 1);
+      mbar_init(smem_u32(&sm.kv_free[i]), 2);
     }
     for (int t = 0; t < 2; ++t) {
       for (int i = 0; i < 2; ++i) {
@@ -277,7 +277,8 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       }
       mbar_init(smem_u32(&sm.o_done[t]), 1);
     }
-    mbar_init(smem_u32(&sm.o_final), 1);
+    mbar_init(smem_u32(&sm.o_final[0]), 1);
+    mbar_init(smem_u32(&sm.o_final[1]), 1);
     mbar_init(smem_u32(&sm.q_ready), 1);
     fence_mbar_init();
   }
@@ -327,48 +328,38 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         bulk_g2s_hint(smem_u32(sm.sf[st][1]), a.v_sf + row * (kD / 16), kScalePage, fb, pol);
       }
     }
-  } else if (warp == 1) {
-    // --------------------------------------------------------- MMA issuer
-    // S_T(j) goes to TMEM buffer j & 1 of M-tile T, so S of tile j+2 is
-    // computed while the softmax works on tile j+1.  P_T(j) is written by the
-    // softmax over the consumed S_T(j) columns (hi and lo, 8 columns each per
-    // 32 keys) and read from there as the A operand of PV.  Issue order per
-    // tile j: PV_0(j), S_0(j+2), PV_1(j), S_1(j+2); a commit after S_T(j+2)
-    // therefore also covers PV_T(j).
-    // The whole warp runs this loop (descriptor arithmetic stays warp-uniform,
-    // which keeps it in the uniform datapath the MMA reads); one elected lane
-    // issues each MMA and commit.  Descriptors are built once and advanced by
-    // adding the byte offset / 16 to their start-address field.
+  } else if (warp == 1 || warp == 3) {
+    // -------------------------------------------------------- MMA issuers
+    // Warp 1 issues every MMA of M-tile 0, warp 3 those of M-tile 1, each in
+    // a fixed order: S_T(0), S_T(1), then per KV tile j: PV_T(j), S_T(j+2).
+    // S_T(j) goes to TMEM buffer j & 1 of the M-tile, so S_T(j+2) is computed
+    // while the softmax works on tile j+1; it overwrites P_T(j), which PV_T(j)
+    // reads -- both come from this thread, and one thread's MMAs run in issue
+    // order.  An issuer waits for K/V readiness before it waits for P (the
+    // dequantisers run ahead, so those waits are normally already satisfied)
+    // and then issues PV_T(j) and S_T(j+2) back to back: the hand-off from
+    // softmax to tensor core is one barrier wait.  Each warp issues for one
+    // M-tile only, keeping its instruction path short on an SM whose issue
+    // slots the softmax and dequant warps keep busy.  KV slot j % kNK is
+    // released when both M-tiles' PV_T(j) have completed (two commits).
+    // The whole warp runs this code (descriptor arithmetic stays
+    // warp-uniform, which keeps it in the uniform datapath the MMA reads);
+    // one elected lane issues each MMA and commit.
+    const int T = warp == 1 ? 0 : 1;
     if (n_tiles > 0) {
       constexpr uint32_t idS = tc::idesc_e4m3_f32(128, kKT, false);  // B = K tile, K-major
       constexpr uint32_t idO = tc::idesc_e4m3_f32(128, 128, true);   // B = V tile, MN-major
-      const uint64_t dq0 = tc::sw128_desc(smem_u32(sm.q[0]));
+      const uint64_t dq = tc::sw128_desc(smem_u32(sm.q[T]));
       const uint64_t dk0 = tc::sw128_desc(smem_u32(sm.k[0]));
       const uint64_t dv0 = tc::sw128_desc(smem_u32(sm.v[0]));
-      const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
-      auto issue_s = [&](int T, int j) {
-        const uint64_t dq = dq0 + (uint64_t)(T * (kQTile >> 4));
+      const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0) + (uint32_t)T * kTmemPerTile;
+      auto issue_s = [&](int j) {
         const uint64_t dk = dk0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
-        const uint32_t d = tm + (uint32_t)T * kTmemPerTile + (uint32_t)(j & 1) * kKT;
+        const uint32_t d = tm + (uint32_t)(j & 1) * kKT;
         if (tc::elect_one()) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) tc::mma_e4m3(d, dq + 2 * k, dk + 2 * k, idS, k > 0);
           tc::commit(smem_u32(&sm.s_full[T][j & 1]));
-        }
-        __syncwarp();
-      };
-      auto issue_pv = [&](int T, int j, bool free_kv) {
-        const uint32_t pa = tm + (uint32_t)T * kTmemPerTile + (uint32_t)(j & 1) * kKT;
-        const uint64_t dv = dv0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
-        const uint32_t d = tm + (uint32_t)T * kTmemPerTile + kTmemO;
-        if (tc::elect_one()) {
-#pragma unroll
-          for (int k = 0; k < kKT / 32; ++k) {
-            tc::mma_e4m3_tmem_a(d, pa + 16 * k, dv + 256 * k, idO, (j > 0 || k > 0) ? 1u : 0u);
-            tc::mma_e4m3_tmem_a(d, pa + 16 * k + 8, dv + 256 * k, idO, 1u);
-          }
-          tc::commit(smem_u32(&sm.o_done[T]));
-          if (free_kv) tc::commit(smem_u32(&sm.kv_free[j % kNK]));
         }
         __syncwarp();
       };
@@ -380,63 +371,38 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         ok = wait_all(&sm.k_ready[j % kNK], (j / kNK) & 1);
         if (!ok) break;
         tc::fence_after_thread_sync();
-        issue_s(0, j);
-        issue_s(1, j);
+        issue_s(j);
       }
-      // Event loop: never block on one M-tile while the other could proceed.
-      // PV_T(j) needs P_T(j) and V_j; S_T(j) needs K_j and PV_T(j-2) issued
-      // (it reuses that S buffer).  KV tile j is released after the second
-      // of its two PVs (a commit covers every MMA issued before it).
-      int nj[2] = {0, 0};                                           // next PV tile
-      int ns[2] = {n_tiles < 2 ? n_tiles : 2, n_tiles < 2 ? n_tiles : 2};  // next S tile
-      int turn = 0;
-      uint64_t t_idle = 0;
-      auto ready = [&](uint64_t* bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_test_wait(smem_u32(bar), parity));
-      };
-      while (ok && (nj[0] < n_tiles || nj[1] < n_tiles)) {
-        bool progressed = false;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int j2 = j + 2;
+        ok = wait_all(&sm.v_ready[j % kNK], (j / kNK) & 1) &&
+             (j2 >= n_tiles || wait_all(&sm.k_ready[j2 % kNK], (j2 / kNK) & 1)) &&
+             wait_all(&sm.p_full[T][j & 1], (j >> 1) & 1);
+        if (!ok) break;
+        tc::fence_after_thread_sync();
+        const uint32_t pa = tm + (uint32_t)(j & 1) * kKT;
+        const uint64_t dv = dv0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int probe = 0; probe < 2; ++probe) {
-          const int c = turn ^ probe;
-          const int j = nj[c];
-          if (j < n_tiles && j < ns[c] && ready(&sm.p_full[c][j & 1], (j >> 1) & 1) &&
-              ready(&sm.v_ready[j % kNK], (j / kNK) & 1)) {
-            tc::fence_after_thread_sync();
-            issue_pv(c, j, nj[c ^ 1] > j);
-            nj[c] = j + 1;
-            progressed = true;
+          for (int k = 0; k < kKT / 32; ++k) {
+            tc::mma_e4m3_tmem_a(tm + kTmemO, pa + 16 * k, dv + 256 * k, idO, (j > 0 || k > 0) ? 1u : 0u);
+            tc::mma_e4m3_tmem_a(tm + kTmemO, pa + 16 * k + 8, dv + 256 * k, idO, 1u);
           }
-          const int js = ns[c];
-          if (js < n_tiles && js < nj[c] + 2 && ready(&sm.k_ready[js % kNK], (js / kNK) & 1)) {
-            tc::fence_after_thread_sync();
-            issue_s(c, js);
-            ns[c] = js + 1;
-            progressed = true;
-          }
+          tc::commit(smem_u32(&sm.o_done[T]));
+          tc::commit(smem_u32(&sm.kv_free[j % kNK]));
         }
-        turn ^= 1;
-        if (progressed) {
-          t_idle = 0;
-        } else {
-          const uint64_t now = global_timer_ns();
-          if (t_idle == 0) t_idle = now;
-          if (now - t_idle > kWaitNs) {
-            if (lane == 0) atomicOr(&g_ctx_err, kErrWaitTimeout);
-            ok = false;
-          }
-          __nanosleep(128);
-        }
+        __syncwarp();
+        if (j2 < n_tiles) issue_s(j2);
       }
-      if (tc::elect_one()) tc::commit(smem_u32(&sm.o_final));
+      if (tc::elect_one()) tc::commit(smem_u32(&sm.o_final[T]));
       __syncwarp();
     }
-  } else if (warp < 4) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------ Q loader
     // One TMA box per M-tile: [32 queries][4 heads][128 d] = rows r = 4*query
     // + head, 128-byte swizzled by the tensor map.  Rows past total_q read as
     // zero; rows of the next sequence are computed but never stored.
-    if (warp == 2 && lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_tiles > 0) {
       const uint32_t qb_ = smem_u32(&sm.q_ready);
       mbar_arrive_expect_tx(qb_, 2u * kQTile);
       tma_load_3d(smem_u32(sm.q[0]), &q_map, 0, g * kGroup, qo + q0, qb_);
@@ -575,7 +541,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     // ------------------------------------------------------------ epilogue
     bool have_o = false;
     if (ok && n_tiles > 0) {
-      have_o = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_final), 0, &g_ctx_err));
+      have_o = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_final[T]), 0, &g_ctx_err));
       tc::fence_after_thread_sync();
     }
     const float inv = (l > 0.f) ? inv_out_scale / l : 0.f;
