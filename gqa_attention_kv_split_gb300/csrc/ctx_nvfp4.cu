@@ -24,22 +24,23 @@
 //    MMA issuers of M-tile 0 and 1 (warp 1 also owns the TMEM allocation);
 //    2 = Q loader (two TMA boxes through a 128-byte-swizzling tensor map);
 //    4-7 and 8-11 = softmax of M-tile 0 and 1 (one thread per TMEM lane =
-//    row); 12-15 = dequantisers writing E4M3 K and V tiles in the 128-byte
-//    swizzled layout the MMA descriptors read (K as the K-major B operand of
-//    S = Q K^T, V as the MN-major B operand of O = P V).
+//    row); 12-15 = dequantisers writing the K tile (E4M3) and the V tile
+//    (its E4M3 values widened to F16) in the 128-byte swizzled layouts the
+//    MMA descriptors read (K as the K-major B operand of S = Q K^T, V as the
+//    MN-major B operand of O = P V).
 //  * MMA order of M-tile T per KV tile j: PV_T(j), S_T(j+2).  A softmax warp
 //    that raises its running maximum waits for the PV of the previous tile
 //    (o_done) before rescaling O in TMEM.
 //  * Online softmax in the exp2 domain with a lazy running maximum m: m is
-//    raised only when a row's maximum exceeds it by more than 2^4, so O is
-//    rescaled rarely.  P = 2^(x - m + 4) <= 2^8 stays inside E4M3, and the
-//    +4 lifts the weights that matter out of E4M3's subnormal range (below
-//    2^-6), where a split term would lose its relative precision.
-//  * P enters the FP8 PV product as two E4M3 terms, P_hi (P truncated to
-//    E4M3 precision) and P_lo = E4M3(P - P_hi), each multiplied by V into the
-//    same TMEM accumulator.  One E4M3 term alone carries ~2 % relative error
-//    per weight, which shows in the output after its own E4M3 rounding; the
-//    pair carries ~2^-7.
+//    raised only when a row's maximum exceeds it by more than 2^8, so O is
+//    rescaled rarely, and P = 2^(x - m) <= 2^8.
+//  * S = Q K^T is an FP8 (E4M3 x E4M3) product.  P V is an F16 product: P is
+//    rounded to f16 (11 significant bits) and V's dequantised E4M3 values
+//    are widened to f16 exactly.  A one-term E4M3 P carries ~2 % relative
+//    error per weight, which puts ~3 % of the outputs more than 2 E4M3 ulps
+//    from the exact result; an f16 P costs no more tensor time than the
+//    two E4M3 terms (hi + lo) it would take to match it, and one conversion
+//    per two weights instead of a split.
 #include <cuda.h>  // CUtensorMap and the cuTensorMapEncodeTiled prototype (resolved at run time)
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -99,11 +100,11 @@ constexpr int kNK = 4;                     // E4M3 K/V tile slots
 constexpr int kNP = 6;                     // packed-page ring stages
 constexpr int kCtxThreads = 512;
 constexpr int kQTile = 128 * 128;          // one M-tile of Q, E4M3: 16 KB
-constexpr int kKVTile = kKT * 128;         // one K or V tile, E4M3: 8 KB
+constexpr int kKVTile = kKT * 128;         // one K tile, E4M3: 8 KB
+constexpr int kVHalf = kKT * 64 * 2;       // one V tile half (64 of the 128 d), F16: 8 KB
 constexpr int kPackedPage = kPage * kD / 2;   // 4 KB of codes per (page, KV head)
 constexpr int kScalePage = kPage * kD / 16;   // 512 B of scales per (page, KV head)
-constexpr float kRescaleLog2 = 4.f;        // lazy-maximum threshold
-constexpr float kPBiasLog2 = 4.f;          // P = 2^(x - m + 4): P <= 2^(4 + 4) = 256 < 448
+constexpr float kRescaleLog2 = 8.f;        // lazy-maximum threshold: P = 2^(x - m) <= 2^8
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns of M-tile T: S buffers at T*256 + {0, 64}, O at T*256 + 128.
 constexpr uint32_t kTmemPerTile = 256;
@@ -112,7 +113,7 @@ constexpr uint32_t kTmemO = 128;
 struct CtxSmem {
   uint8_t q[2][kQTile];        // M-tiles 0/1 of Q (128B-swizzled, K-major A operand)
   uint8_t k[kNK][kKVTile];     // E4M3 K tiles (128B-swizzled, K-major B operand of S = Q K^T)
-  uint8_t v[kNK][kKVTile];     // E4M3 V tiles (128B-swizzled, MN-major B operand of O += P V)
+  uint8_t v[kNK][2 * kVHalf];  // V tiles as F16 (128B-swizzled, MN-major B operand of O += P V; d 0-63, then 64-127)
   uint8_t pk[kNP][2][kPackedPage];  // [stage][K=0,V=1][slot*64 + byte]
   uint8_t sf[kNP][2][kScalePage];   // [stage][K,V][slot*8 + block]
   uint64_t pk_full[kNP], pk_empty[kNP];
@@ -169,19 +170,6 @@ __device__ void find_unit(const int32_t* __restrict__ qo, int B, int t, int& out
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
-// p with its f32 mantissa cut to E4M3's 3 bits (exact E4M3 value for
-// 2^-6 <= p <= 448; below that the conversion rounds further).
-__device__ __forceinline__ float trunc_e4m3(float p) { return __uint_as_float(__float_as_uint(p) & 0xFFF00000u); }
-
-// Four floats -> four E4M3 bytes (e0 in the low byte), rounding toward zero,
-// saturating.  The stochastic-rounding conversion with all random bits zero
-// truncates; one instruction packs all four bytes.
-__device__ __forceinline__ uint32_t e4m3x4_rz(float e0, float e1, float e2, float e3) {
-  uint32_t r;
-  asm("cvt.rs.satfinite.e4m3x4.f32 %0, {%1, %2, %3, %4}, %5;" : "=r"(r) : "f"(e3), "f"(e2), "f"(e1), "f"(e0), "r"(0u));
-  return r;
-}
-
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -192,28 +180,13 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
   asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-// 2^x on two f16 values at once.
-__device__ __forceinline__ uint32_t ex2_h2(uint32_t x) {
-  uint32_t y;
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-__device__ __forceinline__ uint32_t hadd2_u(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 // Two E4M3 bytes (low 16 bits, first element low) -> f16x2 (exact).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
   uint32_t d;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)v));
   return d;
 }
+// Two floats -> f16x2 (lo in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -232,14 +205,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 // Two floats -> two E4M3 bytes (x in the low byte), RNE, satfinite.
 __device__ __forceinline__ uint32_t f2_to_e4m3x2(float lo, float hi) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
-
-// ph = (p0, p1) as f16x2 -> hi = E4M3(p) and lo = E4M3(p - hi), two bytes
-// each (p0 low).  ph - hi is exact in f16: hi lies within a factor 1 +- 2^-4
-// of ph, or both sit on the 2^-9 grid of E4M3's subnormal range.
-__device__ __forceinline__ void split_e4m3x2(uint32_t ph, uint32_t& hi, uint32_t& lo) {
-  hi = f16x2_to_e4m3x2(ph);
-  lo = f16x2_to_e4m3x2(hsub2_u(ph, e4m3x2_to_f16x2(hi)));
 }
 
 __global__ void __launch_bounds__(kCtxThreads, 1)
@@ -348,10 +313,10 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     const int T = warp == 1 ? 0 : 1;
     if (n_tiles > 0) {
       constexpr uint32_t idS = tc::idesc_e4m3_f32(128, kKT, false);  // B = K tile, K-major
-      constexpr uint32_t idO = tc::idesc_e4m3_f32(128, 128, true);   // B = V tile, MN-major
+      constexpr uint32_t idO = tc::idesc_f16_f32(128, 128, true);    // B = V tile (F16), MN-major
       const uint64_t dq = tc::sw128_desc(smem_u32(sm.q[T]));
       const uint64_t dk0 = tc::sw128_desc(smem_u32(sm.k[0]));
-      const uint64_t dv0 = tc::sw128_desc(smem_u32(sm.v[0]));
+      const uint64_t dv0 = tc::sw128_desc_lbo(smem_u32(sm.v[0]), kVHalf);
       const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0) + (uint32_t)T * kTmemPerTile;
       auto issue_s = [&](int j) {
         const uint64_t dk = dk0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
@@ -381,13 +346,12 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         if (!ok) break;
         tc::fence_after_thread_sync();
         const uint32_t pa = tm + (uint32_t)(j & 1) * kKT;
-        const uint64_t dv = dv0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
+        const uint64_t dv = dv0 + (uint64_t)((j % kNK) * ((2 * kVHalf) >> 4));
         if (tc::elect_one()) {
+          // K = 16 keys per MMA: 8 TMEM columns of P, 16 rows (2048 B) of V
 #pragma unroll
-          for (int k = 0; k < kKT / 32; ++k) {
-            tc::mma_e4m3_tmem_a(tm + kTmemO, pa + 16 * k, dv + 256 * k, idO, (j > 0 || k > 0) ? 1u : 0u);
-            tc::mma_e4m3_tmem_a(tm + kTmemO, pa + 16 * k + 8, dv + 256 * k, idO, 1u);
-          }
+          for (int k = 0; k < kKT / 16; ++k)
+            tc::mma_f16_tmem_a(tm + kTmemO, pa + 8 * k, dv + 128 * k, idO, (j > 0 || k > 0) ? 1u : 0u);
           tc::commit(smem_u32(&sm.o_done[T]));
           tc::commit(smem_u32(&sm.kv_free[j % kNK]));
         }
@@ -494,41 +458,29 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         l *= alpha;
         m_used = m_new;
       }
-      // pass 2: P = 2^(x - m_used + 4) (f32 ex2), split into E4M3 hi + lo and
-      // stored over the consumed S columns: keys 32c..32c+31 -> hi at columns
-      // 16c..16c+7, lo at 16c+8..16c+15 (4 keys per column).  hi is P
-      // truncated to E4M3's 3 mantissa bits, lo = P - hi (exact in f32) is
-      // itself truncated to E4M3: hi + lo carries P to within 2^-7 of its
-      // value, always from below.  Masked keys (and every key of a row that
-      // has seen none) become 2^-inf = 0.
+      // pass 2: P = 2^(x - m_used) (f32 ex2) <= 2^8, rounded to f16 and
+      // stored over the consumed S columns as the A operand of the F16 PV
+      // product: keys 32c..32c+31 -> columns 16c..16c+15, two keys per
+      // column.  l sums the unrounded P.  Masked keys (and every key of a
+      // row that has seen none) become 2^-inf = 0.
       const float2 cc = make_float2(scale_log2, scale_log2);
-      const float2 mm = make_float2(kPBiasLog2 - m_used, kPBiasLog2 - m_used);
+      const float2 mm = make_float2(-m_used, -m_used);
       float2 lacc = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < kKT / 32; ++c) {
         const uint32_t* v = c == 0 ? v0 : v1;
-        uint32_t pp[16];  // [0..7] hi, [8..15] lo
+        uint32_t pp[16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {  // keys 4q .. 4q+3 of the chunk
-          float2 x01 = __ffma2_rn(make_float2(u2f(v[4 * q]), u2f(v[4 * q + 1])), cc, mm);
-          float2 x23 = __ffma2_rn(make_float2(u2f(v[4 * q + 2]), u2f(v[4 * q + 3])), cc, mm);
+        for (int q = 0; q < 16; ++q) {  // keys 2q, 2q+1 of the chunk
+          float2 x = __ffma2_rn(make_float2(u2f(v[2 * q]), u2f(v[2 * q + 1])), cc, mm);
           if (masked) {
-            const int k0 = kbase + 32 * c + 4 * q;
-            if (k0 > lim) x01.x = -INFINITY;
-            if (k0 + 1 > lim) x01.y = -INFINITY;
-            if (k0 + 2 > lim) x23.x = -INFINITY;
-            if (k0 + 3 > lim) x23.y = -INFINITY;
+            const int k0 = kbase + 32 * c + 2 * q;
+            if (k0 > lim) x.x = -INFINITY;
+            if (k0 + 1 > lim) x.y = -INFINITY;
           }
-          const float2 p01 = make_float2(fast_exp2(x01.x), fast_exp2(x01.y));
-          const float2 p23 = make_float2(fast_exp2(x23.x), fast_exp2(x23.y));
-          lacc = __fadd2_rn(lacc, p01);
-          lacc = __fadd2_rn(lacc, p23);
-          const float2 h01 = make_float2(trunc_e4m3(p01.x), trunc_e4m3(p01.y));
-          const float2 h23 = make_float2(trunc_e4m3(p23.x), trunc_e4m3(p23.y));
-          const float2 l01 = __ffma2_rn(h01, make_float2(-1.f, -1.f), p01);
-          const float2 l23 = __ffma2_rn(h23, make_float2(-1.f, -1.f), p23);
-          pp[q] = e4m3x4_rz(h01.x, h01.y, h23.x, h23.y);
-          pp[8 + q] = e4m3x4_rz(l01.x, l01.y, l23.x, l23.y);
+          const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          lacc = __fadd2_rn(lacc, pr);
+          pp[q] = f2_to_h2(pr.x, pr.y);
         }
         tc::st16(tS + 16 * c, pp);
       }
@@ -571,34 +523,60 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- dequantisers
-    // Tile j (64 keys): K then V, 512 items of (key, 16-element block) each.
+    // Tile j (64 keys): K then V, 512 items of (key, 16-element block) each,
+    // 4 of each per thread.  All 8 items' codes, scale bytes and scale-table
+    // entries are loaded before the wait for the K/V slot (those loads only
+    // need the packed stage), so their latencies overlap one another and the
+    // wait; K is then written and published before V.
     const int dt = threadIdx.x - 384;
+    const int key0 = dt >> 3;  // items dt + 128 it: key = key0 + 16 it, block = dt & 7
+    const int blk = dt & 7;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % kNP;
       const int slot = j % kNK;
       if (!mbar_wait(smem_u32(&sm.pk_full[st]), (j / kNP) & 1, &g_ctx_err)) break;
-      if (j >= kNK && !mbar_wait(smem_u32(&sm.kv_free[slot]), ((j / kNK) - 1) & 1, &g_ctx_err)) break;
+      uint2 packed[2][4], tab[2][4];
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
-        uint8_t* dst = kv == 0 ? sm.k[slot] : sm.v[slot];
 #pragma unroll
-        for (int it = 0; it < kKT * 8 / 128; ++it) {
-          const int i = dt + 128 * it;  // item = (key, 16-element block)
-          const int key = i >> 3;
-          const int blk = i & 7;
-          uint4 out = make_uint4(0u, 0u, 0u, 0u);
-          if (j * kKT + key < kv_len) {
-            const uint2 packed = *reinterpret_cast<const uint2*>(&sm.pk[st][kv][key * 64 + blk * 8]);
-            out = dequant16_table(packed, sm.sftab[sm.sf[st][kv][key * 8 + blk]]);
-          }
-          *reinterpret_cast<uint4*>(dst + swz(key, blk)) = out;
+        for (int it = 0; it < 4; ++it) {
+          const int key = key0 + 16 * it;
+          packed[kv][it] = *reinterpret_cast<const uint2*>(&sm.pk[st][kv][key * 64 + blk * 8]);
+          tab[kv][it] = sm.sftab[sm.sf[st][kv][key * 8 + blk]];
         }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(kv == 0 ? &sm.k_ready[slot] : &sm.v_ready[slot]));
       }
+      if (j >= kNK && !mbar_wait(smem_u32(&sm.kv_free[slot]), ((j / kNK) - 1) & 1, &g_ctx_err)) break;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int key = key0 + 16 * it;
+        uint4 out = dequant16_table(packed[0][it], tab[0][it]);
+        if (j * kKT + key >= kv_len) out = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sm.k[slot] + swz(key, blk)) = out;
+      }
+      tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.pk_empty[st]));
+      if (lane == 0) mbar_arrive(smem_u32(&sm.k_ready[slot]));
+      // V: d = 16 blk .. 16 blk + 15 -> half blk / 4, 16-byte chunks 2 (blk % 4) and 2 (blk % 4) + 1
+      uint8_t* half = sm.v[slot] + (blk >> 2) * kVHalf;
+      const int c0 = 2 * (blk & 3);
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int key = key0 + 16 * it;
+        uint4 out = dequant16_table(packed[1][it], tab[1][it]);
+        if (j * kKT + key >= kv_len) out = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(half + swz(key, c0)) =
+            make_uint4(e4m3x2_to_f16x2(out.x), e4m3x2_to_f16x2(out.x >> 16), e4m3x2_to_f16x2(out.y),
+                       e4m3x2_to_f16x2(out.y >> 16));
+        *reinterpret_cast<uint4*>(half + swz(key, c0 + 1)) =
+            make_uint4(e4m3x2_to_f16x2(out.z), e4m3x2_to_f16x2(out.z >> 16), e4m3x2_to_f16x2(out.w),
+                       e4m3x2_to_f16x2(out.w >> 16));
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sm.v_ready[slot]));
+        mbar_arrive(smem_u32(&sm.pk_empty[st]));
+      }
     }
   }
 

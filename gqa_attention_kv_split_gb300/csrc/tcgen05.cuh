@@ -49,6 +49,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
   return d;
 }
 
+// The same layout with the atoms along the leading dimension `lbo` bytes
+// apart (bits 16-29): an MN-major operand whose MN extent spans several
+// 128-byte atoms, e.g. 128 16-bit elements = two atoms.
+__device__ __forceinline__ uint64_t sw128_desc_lbo(uint32_t smem_addr, uint32_t lbo) {
+  return (sw128_desc(smem_addr) & ~((uint64_t)0x3FFFu << 16)) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16);
+}
+
 // One lane of the (converged) warp returns true.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
@@ -65,6 +72,13 @@ __device__ __forceinline__ bool elect_one() {
 //   (0 = E4M3); 15 A major (0 = K); 16 B major (0 = K, 1 = MN);
 //   17-22 N >> 3; 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n, bool b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((n >> 3) << 17) |
+         ((m >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16, F16 x F16 -> F32, dense: the same
+// fields, with A/B format code 0 meaning F16 for this kind.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t m, uint32_t n, bool b_mn_major) {
   return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((n >> 3) << 17) |
          ((m >> 4) << 24);
 }
@@ -88,6 +102,19 @@ __device__ __forceinline__ void mma_e4m3_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: one K=16 step of F16
+// operands, A read from 8 TMEM columns holding 2 elements per column
+// (element 2i in the low half).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
