@@ -47,6 +47,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <type_traits>
 #include <cmath>
 #include <mutex>
 
@@ -466,23 +467,34 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       const float2 cc = make_float2(scale_log2, scale_log2);
       const float2 mm = make_float2(-m_used, -m_used);
       float2 lacc = make_float2(0.f, 0.f);
+      // Two copies of the loop, so that the common unmasked tile carries no
+      // per-key mask test.  The choice is made per warp (any lane masked):
+      // the TMEM stores inside are warp-collective and must not diverge.
+      auto pass2 = [&](auto masked_tile) {
+        constexpr bool kMasked = decltype(masked_tile)::value;
 #pragma unroll
-      for (int c = 0; c < kKT / 32; ++c) {
-        const uint32_t* v = c == 0 ? v0 : v1;
-        uint32_t pp[16];
+        for (int c = 0; c < kKT / 32; ++c) {
+          const uint32_t* v = c == 0 ? v0 : v1;
+          uint32_t pp[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {  // keys 2q, 2q+1 of the chunk
-          float2 x = __ffma2_rn(make_float2(u2f(v[2 * q]), u2f(v[2 * q + 1])), cc, mm);
-          if (masked) {
-            const int k0 = kbase + 32 * c + 2 * q;
-            if (k0 > lim) x.x = -INFINITY;
-            if (k0 + 1 > lim) x.y = -INFINITY;
+          for (int q = 0; q < 16; ++q) {  // keys 2q, 2q+1 of the chunk
+            float2 x = __ffma2_rn(make_float2(u2f(v[2 * q]), u2f(v[2 * q + 1])), cc, mm);
+            if (kMasked) {
+              const int k0 = kbase + 32 * c + 2 * q;
+              if (k0 > lim) x.x = -INFINITY;
+              if (k0 + 1 > lim) x.y = -INFINITY;
+            }
+            const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            lacc = __fadd2_rn(lacc, pr);
+            pp[q] = f2_to_h2(pr.x, pr.y);
           }
-          const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          lacc = __fadd2_rn(lacc, pr);
-          pp[q] = f2_to_h2(pr.x, pr.y);
+          tc::st16(tS + 16 * c, pp);
         }
-        tc::st16(tS + 16 * c, pp);
+      };
+      if (__any_sync(0xffffffffu, masked)) {
+        pass2(std::true_type{});
+      } else {
+        pass2(std::false_type{});
       }
       l += lacc.x + lacc.y;
       tc::st_wait();
@@ -546,11 +558,12 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         }
       }
       if (j >= kNK && !mbar_wait(smem_u32(&sm.kv_free[slot]), ((j / kNK) - 1) & 1, &g_ctx_err)) break;
+      const bool tail = (j + 1) * kKT > kv_len;  // keys past kv_len (last tile only) read as zero
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         const int key = key0 + 16 * it;
         uint4 out = dequant16_table(packed[0][it], tab[0][it]);
-        if (j * kKT + key >= kv_len) out = make_uint4(0u, 0u, 0u, 0u);
+        if (tail && j * kKT + key >= kv_len) out = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(sm.k[slot] + swz(key, blk)) = out;
       }
       tc::fence_proxy_async_smem();
@@ -563,7 +576,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       for (int it = 0; it < 4; ++it) {
         const int key = key0 + 16 * it;
         uint4 out = dequant16_table(packed[1][it], tab[1][it]);
-        if (j * kKT + key >= kv_len) out = make_uint4(0u, 0u, 0u, 0u);
+        if (tail && j * kKT + key >= kv_len) out = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(half + swz(key, c0)) =
             make_uint4(e4m3x2_to_f16x2(out.x), e4m3x2_to_f16x2(out.x >> 16), e4m3x2_to_f16x2(out.y),
                        e4m3x2_to_f16x2(out.y >> 16));
