@@ -43,7 +43,6 @@
 //    per two weights instead of a split.
 #include <cuda.h>  // CUtensorMap and the cuTensorMapEncodeTiled prototype (resolved at run time)
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -203,9 +202,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Two floats -> two E4M3 bytes (x in the low byte), RNE, satfinite.
-__device__ __forceinline__ uint32_t f2_to_e4m3x2(float lo, float hi) {
-  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+// Four floats -> four E4M3 bytes (e0 in the low byte), round to nearest
+// even, saturating to +-448: two hardware conversions of two values each
+// (the first source operand lands in the upper byte).
+__device__ __forceinline__ uint32_t f4_to_e4m3x4(float e0, float e1, float e2, float e3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
+  return r;
 }
 
 __global__ void __launch_bounds__(kCtxThreads, 1)
@@ -522,11 +530,12 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         for (int i = 0; i < 32; ++i) o[i] = 0u;
       }
       uint32_t pk[8];
+      const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t lo = f2_to_e4m3x2(u2f(o[4 * i]) * inv, u2f(o[4 * i + 1]) * inv);
-        const uint32_t hi = f2_to_e4m3x2(u2f(o[4 * i + 2]) * inv, u2f(o[4 * i + 3]) * inv);
-        pk[i] = lo | (hi << 16);
+        const float2 a = __fmul2_rn(make_float2(u2f(o[4 * i]), u2f(o[4 * i + 1])), inv2);
+        const float2 b = __fmul2_rn(make_float2(u2f(o[4 * i + 2]), u2f(o[4 * i + 3])), inv2);
+        pk[i] = f4_to_e4m3x4(a.x, a.y, b.x, b.y);
       }
       if (store) {
         *reinterpret_cast<uint4*>(dst + 32 * c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
