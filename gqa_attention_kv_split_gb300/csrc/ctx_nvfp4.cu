@@ -104,7 +104,8 @@ constexpr int kKVTile = kKT * 128;         // one K tile, E4M3: 8 KB
 constexpr int kVHalf = kKT * 64 * 2;       // one V tile half (64 of the 128 d), F16: 8 KB
 constexpr int kPackedPage = kPage * kD / 2;   // 4 KB of codes per (page, KV head)
 constexpr int kScalePage = kPage * kD / 16;   // 512 B of scales per (page, KV head)
-constexpr float kRescaleLog2 = 8.f;        // lazy-maximum threshold: P = 2^(x - m) <= 2^8
+constexpr float kRescaleLog2 = 8.f;        // lazy-maximum threshold when a row's maximum is recomputed
+constexpr float kMaxTileSum = 32768.f;     // a tile's row sum of P up to which no P can overflow f16
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns of M-tile T: S buffers at T*256 + {0, 64}, O at T*256 + 128.
 constexpr uint32_t kTmemPerTile = 256;
@@ -407,15 +408,56 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       const uint32_t tS = tT + (uint32_t)(j & 1) * kKT;
       const int kbase = j * kKT;
       const bool masked = kbase + kKT - 1 > lim;
-      // pass 1: extreme raw logit of the row (max, or min for a negative
-      // scale), then the scaled maximum in the exp2 domain
-      float ext = neg_scale ? INFINITY : -INFINITY;
-      // the tile's 64 logits stay in registers for both passes
+      // the tile's 64 logits stay in registers
       uint32_t v0[32], v1[32];
       tc::ld32(tS, v0);
       tc::ld32(tS + 32, v1);
       tc::ld_wait();
-      {
+      const bool mask_warp = __any_sync(0xffffffffu, masked);
+      // P = 2^(x - m_used), rounded to f16 and stored over the consumed S
+      // columns as the A operand of the F16 PV product: keys 32c..32c+31 ->
+      // columns 16c..16c+15, two keys per column.  Returns the row's sum of
+      // the unrounded P.  Masked keys (and every key of a row that has seen
+      // none) become 2^-inf = 0.  Two copies of the loop, so that the common
+      // unmasked tile carries no per-key mask test; the choice is made per
+      // warp (any lane masked): the TMEM stores are warp-collective and must
+      // not diverge.
+      auto pass_p = [&](auto masked_tile) {
+        constexpr bool kMasked = decltype(masked_tile)::value;
+        const float2 cc = make_float2(scale_log2, scale_log2);
+        const float2 mm = make_float2(-m_used, -m_used);
+        float2 lacc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < kKT / 32; ++c) {
+          const uint32_t* v = c == 0 ? v0 : v1;
+          uint32_t pp[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {  // keys 2q, 2q+1 of the chunk
+            float2 x = __ffma2_rn(make_float2(u2f(v[2 * q]), u2f(v[2 * q + 1])), cc, mm);
+            if (kMasked) {
+              const int k0 = kbase + 32 * c + 2 * q;
+              if (k0 > lim) x.x = -INFINITY;
+              if (k0 + 1 > lim) x.y = -INFINITY;
+            }
+            const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            lacc = __fadd2_rn(lacc, pr);
+            pp[q] = f2_to_h2(pr.x, pr.y);
+          }
+          tc::st16(tS + 16 * c, pp);
+        }
+        return lacc.x + lacc.y;
+      };
+      // Optimistic pass with the running maximum as it stands.  A row sum of
+      // at most 2^15 bounds every P of the row by 2^15 < 65504, so the f16
+      // values are finite and the tile is done.  Otherwise (a row's first
+      // keys, where m_used is -inf, or a maximum that grew by more than ~9) the
+      // warp finds the rows' maxima, raises m where it grew by more than
+      // 2^kRescaleLog2 (rescaling O and l), and computes P again.
+      float lsum = mask_warp ? pass_p(std::true_type{}) : pass_p(std::false_type{});
+      if (__any_sync(0xffffffffu, !(lsum <= kMaxTileSum))) {
+        // extreme raw logit of the row (max, or min for a negative scale),
+        // then the scaled maximum in the exp2 domain
+        float ext = neg_scale ? INFINITY : -INFINITY;
         if (!masked) {
           float e0 = ext, e1 = u2f(v0[0]), e2 = u2f(v1[0]), e3 = u2f(v1[1]);
           if (!neg_scale) {
@@ -440,71 +482,36 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
             if (kbase + 32 + i <= lim) ext = neg_scale ? fminf(ext, u2f(v1[i])) : fmaxf(ext, u2f(v1[i]));
           }
         }
-      }
-      const float mx = (ext == INFINITY || ext == -INFINITY) ? -INFINITY : ext * scale_log2;
-      const float m_new = fmaxf(m_used, mx);
-      const bool raise = m_new > m_used + kRescaleLog2;  // also true for the first finite maximum
-      const float alpha = raise ? fast_exp2(m_used - m_new) : 1.f;  // 0 when m_used was -inf
-      if (__any_sync(0xffffffffu, raise && j > 0)) {
-        // O_T must hold PV of every tile < j before it is rescaled
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_done[T]), (j - 1) & 1, &g_ctx_err))) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_thread_sync();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tc::ld32(tO + 32 * c, o);
-          tc::ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(u2f(o[i]) * alpha);
-          tc::st32(tO + 32 * c, o);
-        }
-        tc::st_wait();
-      }
-      if (raise) {
-        l *= alpha;
-        m_used = m_new;
-      }
-      // pass 2: P = 2^(x - m_used) (f32 ex2) <= 2^8, rounded to f16 and
-      // stored over the consumed S columns as the A operand of the F16 PV
-      // product: keys 32c..32c+31 -> columns 16c..16c+15, two keys per
-      // column.  l sums the unrounded P.  Masked keys (and every key of a
-      // row that has seen none) become 2^-inf = 0.
-      const float2 cc = make_float2(scale_log2, scale_log2);
-      const float2 mm = make_float2(-m_used, -m_used);
-      float2 lacc = make_float2(0.f, 0.f);
-      // Two copies of the loop, so that the common unmasked tile carries no
-      // per-key mask test.  The choice is made per warp (any lane masked):
-      // the TMEM stores inside are warp-collective and must not diverge.
-      auto pass2 = [&](auto masked_tile) {
-        constexpr bool kMasked = decltype(masked_tile)::value;
-#pragma unroll
-        for (int c = 0; c < kKT / 32; ++c) {
-          const uint32_t* v = c == 0 ? v0 : v1;
-          uint32_t pp[16];
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {  // keys 2q, 2q+1 of the chunk
-            float2 x = __ffma2_rn(make_float2(u2f(v[2 * q]), u2f(v[2 * q + 1])), cc, mm);
-            if (kMasked) {
-              const int k0 = kbase + 32 * c + 2 * q;
-              if (k0 > lim) x.x = -INFINITY;
-              if (k0 + 1 > lim) x.y = -INFINITY;
-            }
-            const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-            lacc = __fadd2_rn(lacc, pr);
-            pp[q] = f2_to_h2(pr.x, pr.y);
+        const float mx = (ext == INFINITY || ext == -INFINITY) ? -INFINITY : ext * scale_log2;
+        const float m_new = fmaxf(m_used, mx);
+        const bool raise = m_new > m_used + kRescaleLog2;  // also true for the first finite maximum
+        const float alpha = raise ? fast_exp2(m_used - m_new) : 1.f;  // 0 when m_used was -inf
+        if (__any_sync(0xffffffffu, raise && j > 0)) {
+          // O_T must hold PV of every tile < j before it is rescaled
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_done[T]), (j - 1) & 1, &g_ctx_err))) {
+            ok = false;
+            break;
           }
-          tc::st16(tS + 16 * c, pp);
+          tc::fence_after_thread_sync();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tc::ld32(tO + 32 * c, o);
+            tc::ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(u2f(o[i]) * alpha);
+            tc::st32(tO + 32 * c, o);
+          }
+          tc::st_wait();
         }
-      };
-      if (__any_sync(0xffffffffu, masked)) {
-        pass2(std::true_type{});
-      } else {
-        pass2(std::false_type{});
+        if (raise) {
+          l *= alpha;
+          m_used = m_new;
+        }
+        tc::st_wait();  // the optimistic P stores complete before they are overwritten
+        lsum = mask_warp ? pass_p(std::true_type{}) : pass_p(std::false_type{});
       }
-      l += lacc.x + lacc.y;
+      l += lsum;
       tc::st_wait();
       tc::fence_before_thread_sync();
       __syncwarp();
