@@ -118,7 +118,7 @@ struct CtxSmem {
   uint8_t pk[kNP][2][kPackedPage];  // [stage][K=0,V=1][slot*64 + byte]
   uint8_t sf[kNP][2][kScalePage];   // [stage][K,V][slot*8 + block]
   uint64_t pk_full[kNP], pk_empty[kNP];
-  uint64_t k_ready[kNK], v_ready[kNK], kv_free[kNK];
+  uint64_t kv_ready[kNK], kv_free[kNK];  // dequantised K and V tile of a slot written / slot consumed
   uint64_t s_full[2][2], p_full[2][2];  // [M-tile][S buffer]
   uint64_t o_done[2];                   // PV of an M-tile completed (one phase per KV tile)
   uint64_t o_final[2], q_ready;  // o_final: every MMA of an M-tile completed
@@ -241,8 +241,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       mbar_init(smem_u32(&sm.pk_empty[i]), 4);
     }
     for (int i = 0; i < kNK; ++i) {
-      mbar_init(smem_u32(&sm.k_ready[i]), 4);
-      mbar_init(smem_u32(&sm.v_ready[i]), 4);
+      mbar_init(smem_u32(&sm.kv_ready[i]), 4);
       mbar_init(smem_u32(&sm.kv_free[i]), 2);
     }
     for (int t = 0; t < 2; ++t) {
@@ -310,16 +309,16 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     // S_T(j) goes to TMEM buffer j & 1 of the M-tile, so S_T(j+2) is computed
     // while the softmax works on tile j+1; it overwrites P_T(j), which PV_T(j)
     // reads -- both come from this thread, and one thread's MMAs run in issue
-    // order.  An issuer waits for K/V readiness before it waits for P (the
-    // dequantisers run ahead, so those waits are normally already satisfied)
-    // and then issues PV_T(j) and S_T(j+2) back to back: the hand-off from
-    // softmax to tensor core is one barrier wait.  Each warp issues for one
-    // M-tile only, keeping its instruction path short on an SM whose issue
-    // slots the softmax and dequant warps keep busy.  KV slot j % kNK is
-    // released when both M-tiles' PV_T(j) have completed (two commits).
-    // The whole warp runs this code (descriptor arithmetic stays
-    // warp-uniform, which keeps it in the uniform datapath the MMA reads);
-    // one elected lane issues each MMA and commit.
+    // order.  Tile j's K and V are published together (kv_ready), waited for
+    // before S_T(j) and hence known ready for PV_T(j).  Per tile the issuer
+    // waits for K/V of tile j+2 first (normally already there: the
+    // dequantisers run ahead) and for P_T(j) last, then issues PV_T(j) and
+    // S_T(j+2) back to back: the hand-off from softmax to tensor core is one
+    // barrier wait.  KV slot j % kNK is released when both M-tiles' PV_T(j)
+    // have completed (two commits).  The whole warp runs this code
+    // (descriptor arithmetic stays warp-uniform, which keeps it in the
+    // uniform datapath the MMA reads); one elected lane issues each MMA and
+    // commit.
     const int T = warp == 1 ? 0 : 1;
     if (n_tiles > 0) {
       constexpr uint32_t idS = tc::idesc_e4m3_f32(128, kKT, false);  // B = K tile, K-major
@@ -343,15 +342,14 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       };
       bool ok = wait_all(&sm.q_ready, 0);
       for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
-        ok = wait_all(&sm.k_ready[j % kNK], (j / kNK) & 1);
+        ok = wait_all(&sm.kv_ready[j % kNK], (j / kNK) & 1);
         if (!ok) break;
         tc::fence_after_thread_sync();
         issue_s(j);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int j2 = j + 2;
-        ok = wait_all(&sm.v_ready[j % kNK], (j / kNK) & 1) &&
-             (j2 >= n_tiles || wait_all(&sm.k_ready[j2 % kNK], (j2 / kNK) & 1)) &&
+        ok = (j2 >= n_tiles || wait_all(&sm.kv_ready[j2 % kNK], (j2 / kNK) & 1)) &&
              wait_all(&sm.p_full[T][j & 1], (j >> 1) & 1);
         if (!ok) break;
         tc::fence_after_thread_sync();
@@ -555,7 +553,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     // 4 of each per thread.  All 8 items' codes, scale bytes and scale-table
     // entries are loaded before the wait for the K/V slot (those loads only
     // need the packed stage), so their latencies overlap one another and the
-    // wait; K is then written and published before V.
+    // wait; K and V are then written and published together.
     const int dt = threadIdx.x - 384;
     const int key0 = dt >> 3;  // items dt + 128 it: key = key0 + 16 it, block = dt & 7
     const int blk = dt & 7;
@@ -582,9 +580,6 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         if (tail && j * kKT + key >= kv_len) out = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(sm.k[slot] + swz(key, blk)) = out;
       }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.k_ready[slot]));
       // V: d = 16 blk .. 16 blk + 15 -> half blk / 4, 16-byte chunks 2 (blk % 4) and 2 (blk % 4) + 1
       uint8_t* half = sm.v[slot] + (blk >> 2) * kVHalf;
       const int c0 = 2 * (blk & 3);
@@ -603,7 +598,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&sm.v_ready[slot]));
+        mbar_arrive(smem_u32(&sm.kv_ready[slot]));
         mbar_arrive(smem_u32(&sm.pk_empty[st]));
       }
     }
