@@ -14,11 +14,12 @@
 //    heads of the group are stacked into the MMA's M dimension: M-tile T
 //    (T = 0, 1) holds queries 32T..32T+31 of the block x 4 heads, row
 //    r = 4 * query + head.  One dequantised K/V tile therefore feeds 256 rows.
-//  * KV tiles of 64 keys (one page).  TMEM (512 columns) per M-tile T: two
-//    S buffers of 64 fp32 columns (S of tile j in buffer j & 1) and O (128
-//    columns), so the MMA computes S(j+2) while the softmax works on tile
-//    j+1.  P is written back over the consumed S columns and read from TMEM
-//    as the A operand of PV.
+//  * KV tiles of 64 keys (one page).  TMEM (512 columns) per M-tile T: S (64
+//    fp32 columns), two P buffers (32 columns each: 64 f16 weights per row)
+//    and O (128 columns).  S of tile j+1 is computed as soon as the softmax
+//    has read S of tile j into registers, i.e. while the softmax works on
+//    tile j; P of tile j goes to P buffer j & 1 and is read from TMEM as the
+//    A operand of PV.
 //  * Warp roles (16 warps): 0 = bulk-copy producer of packed NVFP4 pages +
 //    scales through the block table into a 6-stage ring; 1 and 3 = tcgen05
 //    MMA issuers of M-tile 0 and 1 (warp 1 also owns the TMEM allocation);
@@ -28,12 +29,12 @@
 //    (its E4M3 values widened to F16) in the 128-byte swizzled layouts the
 //    MMA descriptors read (K as the K-major B operand of S = Q K^T, V as the
 //    MN-major B operand of O = P V).
-//  * MMA order of M-tile T per KV tile j: PV_T(j), S_T(j+2).  A softmax warp
+//  * MMA order of M-tile T per KV tile j: S_T(j+1), PV_T(j).  A softmax warp
 //    that raises its running maximum waits for the PV of the previous tile
-//    (o_done) before rescaling O in TMEM.
+//    before rescaling O in TMEM.
 //  * Online softmax in the exp2 domain with a lazy running maximum m: m is
 //    raised only when a row's maximum exceeds it by more than 2^8, so O is
-//    rescaled rarely, and P = 2^(x - m) <= 2^8.
+//    rescaled rarely.
 //  * S = Q K^T is an FP8 (E4M3 x E4M3) product.  P V is an F16 product: P is
 //    rounded to f16 (11 significant bits) and V's dequantised E4M3 values
 //    are widened to f16 exactly.  A one-term E4M3 P carries ~2 % relative
@@ -107,8 +108,11 @@ constexpr int kScalePage = kPage * kD / 16;   // 512 B of scales per (page, KV h
 constexpr float kRescaleLog2 = 8.f;        // lazy-maximum threshold when a row's maximum is recomputed
 constexpr float kMaxTileSum = 32768.f;     // a tile's row sum of P up to which no P can overflow f16
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns of M-tile T: S buffers at T*256 + {0, 64}, O at T*256 + 128.
+// TMEM columns of M-tile T, from T*256: S (64 f32 columns), two P buffers
+// (32 columns of f16 pairs each, tile j in buffer j & 1), O (128 columns).
 constexpr uint32_t kTmemPerTile = 256;
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemP = 64;
 constexpr uint32_t kTmemO = 128;
 
 struct CtxSmem {
@@ -119,8 +123,8 @@ struct CtxSmem {
   uint8_t sf[kNP][2][kScalePage];   // [stage][K,V][slot*8 + block]
   uint64_t pk_full[kNP], pk_empty[kNP];
   uint64_t kv_ready[kNK], kv_free[kNK];  // dequantised K and V tile of a slot written / slot consumed
-  uint64_t s_full[2][2], p_full[2][2];  // [M-tile][S buffer]
-  uint64_t o_done[2];                   // PV of an M-tile completed (one phase per KV tile)
+  uint64_t s_full[2], s_free[2];        // [M-tile]: S computed / S read by the 4 softmax warps
+  uint64_t p_full[2][2], p_free[2][2];  // [M-tile][P buffer]: P written / the PV that read it completed
   uint64_t o_final[2], q_ready;  // o_final: every MMA of an M-tile completed
   uint2 sftab[256];      // E4M3 magnitudes of the 8 E2M1 codes for every scale byte
   uint32_t tmem_base;
@@ -245,11 +249,12 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       mbar_init(smem_u32(&sm.kv_free[i]), 2);
     }
     for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&sm.s_full[t]), 1);
+      mbar_init(smem_u32(&sm.s_free[t]), 4);
       for (int i = 0; i < 2; ++i) {
-        mbar_init(smem_u32(&sm.s_full[t][i]), 1);
         mbar_init(smem_u32(&sm.p_full[t][i]), 4);
+        mbar_init(smem_u32(&sm.p_free[t][i]), 1);
       }
-      mbar_init(smem_u32(&sm.o_done[t]), 1);
     }
     mbar_init(smem_u32(&sm.o_final[0]), 1);
     mbar_init(smem_u32(&sm.o_final[1]), 1);
@@ -304,18 +309,16 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     }
   } else if (warp == 1 || warp == 3) {
     // -------------------------------------------------------- MMA issuers
-    // Warp 1 issues every MMA of M-tile 0, warp 3 those of M-tile 1, each in
-    // a fixed order: S_T(0), S_T(1), then per KV tile j: PV_T(j), S_T(j+2).
-    // S_T(j) goes to TMEM buffer j & 1 of the M-tile, so S_T(j+2) is computed
-    // while the softmax works on tile j+1; it overwrites P_T(j), which PV_T(j)
-    // reads -- both come from this thread, and one thread's MMAs run in issue
-    // order.  Tile j's K and V are published together (kv_ready), waited for
-    // before S_T(j) and hence known ready for PV_T(j).  Per tile the issuer
-    // waits for K/V of tile j+2 first (normally already there: the
-    // dequantisers run ahead) and for P_T(j) last, then issues PV_T(j) and
-    // S_T(j+2) back to back: the hand-off from softmax to tensor core is one
-    // barrier wait.  KV slot j % kNK is released when both M-tiles' PV_T(j)
-    // have completed (two commits).  The whole warp runs this code
+    // Warp 1 issues every MMA of M-tile 0, warp 3 those of M-tile 1, in a
+    // fixed order: S_T(0), then per KV tile j: S_T(j+1), PV_T(j).  S_T(j+1)
+    // overwrites S_T(j) and is issued as soon as the softmax has read S_T(j)
+    // into registers (s_free), so it is computed while the softmax works on
+    // tile j.  P_T(j) goes to P buffer j & 1, which PV_T(j) reads; the
+    // softmax writes P_T(j+2) there only after that PV completed (p_free).
+    // Tile j's K and V are published together (kv_ready), waited for before
+    // S_T(j) and hence known ready for PV_T(j).  KV slot j % kNK is released
+    // when both M-tiles' PV_T(j) have completed (two commits; a commit covers
+    // every MMA its thread issued before it).  The whole warp runs this code
     // (descriptor arithmetic stays warp-uniform, which keeps it in the
     // uniform datapath the MMA reads); one elected lane issues each MMA and
     // commit.
@@ -329,42 +332,43 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0) + (uint32_t)T * kTmemPerTile;
       auto issue_s = [&](int j) {
         const uint64_t dk = dk0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
-        const uint32_t d = tm + (uint32_t)(j & 1) * kKT;
         if (tc::elect_one()) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tc::mma_e4m3(d, dq + 2 * k, dk + 2 * k, idS, k > 0);
-          tc::commit(smem_u32(&sm.s_full[T][j & 1]));
+          for (int k = 0; k < 4; ++k) tc::mma_e4m3(tm + kTmemS, dq + 2 * k, dk + 2 * k, idS, k > 0);
+          tc::commit(smem_u32(&sm.s_full[T]));
         }
         __syncwarp();
       };
       auto wait_all = [&](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, &g_ctx_err));
       };
-      bool ok = wait_all(&sm.q_ready, 0);
-      for (int j = 0; ok && j < 2 && j < n_tiles; ++j) {
-        ok = wait_all(&sm.kv_ready[j % kNK], (j / kNK) & 1);
-        if (!ok) break;
+      bool ok = wait_all(&sm.q_ready, 0) && wait_all(&sm.kv_ready[0], 0);
+      if (ok) {
         tc::fence_after_thread_sync();
-        issue_s(j);
+        issue_s(0);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int j2 = j + 2;
-        ok = (j2 >= n_tiles || wait_all(&sm.kv_ready[j2 % kNK], (j2 / kNK) & 1)) &&
-             wait_all(&sm.p_full[T][j & 1], (j >> 1) & 1);
+        const int j1 = j + 1;
+        if (j1 < n_tiles) {
+          ok = wait_all(&sm.kv_ready[j1 % kNK], (j1 / kNK) & 1) && wait_all(&sm.s_free[T], j & 1);
+          if (!ok) break;
+          tc::fence_after_thread_sync();
+          issue_s(j1);
+        }
+        ok = wait_all(&sm.p_full[T][j & 1], (j >> 1) & 1);
         if (!ok) break;
         tc::fence_after_thread_sync();
-        const uint32_t pa = tm + (uint32_t)(j & 1) * kKT;
+        const uint32_t pa = tm + kTmemP + (uint32_t)(j & 1) * 32;
         const uint64_t dv = dv0 + (uint64_t)((j % kNK) * ((2 * kVHalf) >> 4));
         if (tc::elect_one()) {
           // K = 16 keys per MMA: 8 TMEM columns of P, 16 rows (2048 B) of V
 #pragma unroll
           for (int k = 0; k < kKT / 16; ++k)
             tc::mma_f16_tmem_a(tm + kTmemO, pa + 8 * k, dv + 128 * k, idO, (j > 0 || k > 0) ? 1u : 0u);
-          tc::commit(smem_u32(&sm.o_done[T]));
+          tc::commit(smem_u32(&sm.p_free[T][j & 1]));
           tc::commit(smem_u32(&sm.kv_free[j % kNK]));
         }
         __syncwarp();
-        if (j2 < n_tiles) issue_s(j2);
       }
       if (tc::elect_one()) tc::commit(smem_u32(&sm.o_final[T]));
       __syncwarp();
@@ -391,6 +395,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     if (lim > kv_len - 1) lim = kv_len - 1;
     const uint32_t lane_off = (uint32_t)(32 * sub) << 16;
     const uint32_t tT = tmem + lane_off + (uint32_t)T * kTmemPerTile;
+    const uint32_t tS = tT + kTmemS;
     const uint32_t tO = tT + kTmemO;
     float m_used = -INFINITY;
     float l = 0.f;
@@ -398,19 +403,31 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     const bool neg_scale = scale_log2 < 0.f;
     for (int j = 0; j < n_tiles; ++j) {
       // warp-uniform outcome: the TMEM accesses below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[T][j & 1]), (j >> 1) & 1, &g_ctx_err))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[T]), j & 1, &g_ctx_err))) {
         ok = false;
         break;
       }
       tc::fence_after_thread_sync();
-      const uint32_t tS = tT + (uint32_t)(j & 1) * kKT;
+      const uint32_t tP = tT + kTmemP + (uint32_t)(j & 1) * 32;
       const int kbase = j * kKT;
       const bool masked = kbase + kKT - 1 > lim;
-      // the tile's 64 logits stay in registers
+      // the tile's 64 logits stay in registers; once all four warps have
+      // read them the issuer may compute S of the next tile in their place
       uint32_t v0[32], v1[32];
       tc::ld32(tS, v0);
       tc::ld32(tS + 32, v1);
       tc::ld_wait();
+      tc::fence_before_thread_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.s_free[T]));
+      // P buffer j & 1 was last read by PV of tile j - 2
+      if (j >= 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[T][j & 1]), ((j >> 1) - 1) & 1, &g_ctx_err))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_thread_sync();
+      }
       const bool mask_warp = __any_sync(0xffffffffu, masked);
       // P = 2^(x - m_used), rounded to f16 and stored over the consumed S
       // columns as the A operand of the F16 PV product: keys 32c..32c+31 ->
@@ -441,7 +458,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
             lacc = __fadd2_rn(lacc, pr);
             pp[q] = f2_to_h2(pr.x, pr.y);
           }
-          tc::st16(tS + 16 * c, pp);
+          tc::st16(tP + 16 * c, pp);
         }
         return lacc.x + lacc.y;
       };
@@ -485,8 +502,10 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         const bool raise = m_new > m_used + kRescaleLog2;  // also true for the first finite maximum
         const float alpha = raise ? fast_exp2(m_used - m_new) : 1.f;  // 0 when m_used was -inf
         if (__any_sync(0xffffffffu, raise && j > 0)) {
-          // O_T must hold PV of every tile < j before it is rescaled
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_done[T]), (j - 1) & 1, &g_ctx_err))) {
+          // O_T must hold PV of every tile < j before it is rescaled (the PV
+          // of tile j - 1, the last one issued, has completed)
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[T][(j - 1) & 1]), ((j - 1) >> 1) & 1,
+                                                &g_ctx_err))) {
             ok = false;
             break;
           }
