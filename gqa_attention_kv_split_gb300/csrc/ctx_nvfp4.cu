@@ -21,17 +21,18 @@
 //    tile j; P of tile j goes to P buffer j & 1 and is read from TMEM as the
 //    A operand of PV.
 //  * Warp roles (16 warps): 0 = bulk-copy producer of packed NVFP4 pages +
-//    scales through the block table into a 6-stage ring; 1 and 3 = tcgen05
-//    MMA issuers of M-tile 0 and 1 (warp 1 also owns the TMEM allocation);
-//    2 = Q loader (two TMA boxes through a 128-byte-swizzling tensor map);
-//    4-7 and 8-11 = softmax of M-tile 0 and 1 (one thread per TMEM lane =
-//    row); 12-15 = dequantisers writing the K tile (E4M3) and the V tile
-//    (its E4M3 values widened to F16) in the 128-byte swizzled layouts the
-//    MMA descriptors read (K as the K-major B operand of S = Q K^T, V as the
-//    MN-major B operand of O = P V).
-//  * MMA order of M-tile T per KV tile j: S_T(j+1), PV_T(j).  A softmax warp
-//    that raises its running maximum waits for the PV of the previous tile
-//    before rescaling O in TMEM.
+//    scales through the block table into a 6-stage ring; 1 and 3 = issuers
+//    of S = Q K^T for M-tile 0 and 1 (warp 1 also owns the TMEM allocation);
+//    2 = Q loader (two TMA boxes through a 128-byte-swizzling tensor map),
+//    then issuer of O += P V for both M-tiles; 4-7 and 8-11 = softmax of
+//    M-tile 0 and 1 (one thread per TMEM lane = row); 12-15 = dequantisers
+//    writing the K tile (E4M3) and the V tile (its E4M3 values widened to
+//    F16) in the 128-byte swizzled layouts the MMA descriptors read (K as the
+//    K-major B operand of S = Q K^T, V as the MN-major B operand of O = P V).
+//  * Per M-tile T and KV tile j: S_T(j+1) is issued once the softmax has read
+//    S_T(j); PV_T(j) once it has written P_T(j).  A softmax warp that raises
+//    its running maximum waits for the PV of the previous tile before
+//    rescaling O in TMEM.
 //  * Online softmax in the exp2 domain with a lazy running maximum m: m is
 //    raised only when a row's maximum exceeds it by more than 2^8, so O is
 //    rescaled rarely.
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     }
     for (int i = 0; i < kNK; ++i) {
       mbar_init(smem_u32(&sm.kv_ready[i]), 4);
-      mbar_init(smem_u32(&sm.kv_free[i]), 2);
+      mbar_init(smem_u32(&sm.kv_free[i]), 3);  // S of both M-tiles, PV of both
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&sm.s_full[t]), 1);
@@ -308,73 +309,42 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       }
     }
   } else if (warp == 1 || warp == 3) {
-    // -------------------------------------------------------- MMA issuers
-    // Warp 1 issues every MMA of M-tile 0, warp 3 those of M-tile 1, in a
-    // fixed order: S_T(0), then per KV tile j: S_T(j+1), PV_T(j).  S_T(j+1)
-    // overwrites S_T(j) and is issued as soon as the softmax has read S_T(j)
-    // into registers (s_free), so it is computed while the softmax works on
-    // tile j.  P_T(j) goes to P buffer j & 1, which PV_T(j) reads; the
-    // softmax writes P_T(j+2) there only after that PV completed (p_free).
-    // Tile j's K and V are published together (kv_ready), waited for before
-    // S_T(j) and hence known ready for PV_T(j).  KV slot j % kNK is released
-    // when both M-tiles' PV_T(j) have completed (two commits; a commit covers
-    // every MMA its thread issued before it).  The whole warp runs this code
-    // (descriptor arithmetic stays warp-uniform, which keeps it in the
-    // uniform datapath the MMA reads); one elected lane issues each MMA and
-    // commit.
+    // -------------------------------------------------------- S issuers
+    // Warp 1 issues S = Q K^T of M-tile 0, warp 3 that of M-tile 1: S_T(j)
+    // once K of tile j is dequantised and the softmax has read S_T(j-1) into
+    // registers (s_free), so S of the next tile is computed while the
+    // softmax works on this one.  tcgen05.mma issue blocks while the tensor
+    // pipe is busy, so S and PV have separate issuing warps and an S is
+    // never queued behind a PV the softmax is not waiting for.  The whole
+    // warp runs this code (descriptor arithmetic stays warp-uniform, which
+    // keeps it in the uniform datapath the MMA reads); one elected lane
+    // issues each MMA and commit.
     const int T = warp == 1 ? 0 : 1;
     if (n_tiles > 0) {
       constexpr uint32_t idS = tc::idesc_e4m3_f32(128, kKT, false);  // B = K tile, K-major
-      constexpr uint32_t idO = tc::idesc_f16_f32(128, 128, true);    // B = V tile (F16), MN-major
       const uint64_t dq = tc::sw128_desc(smem_u32(sm.q[T]));
       const uint64_t dk0 = tc::sw128_desc(smem_u32(sm.k[0]));
-      const uint64_t dv0 = tc::sw128_desc_lbo(smem_u32(sm.v[0]), kVHalf);
       const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0) + (uint32_t)T * kTmemPerTile;
-      auto issue_s = [&](int j) {
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, &g_ctx_err));
+      };
+      bool ok = wait_all(&sm.q_ready, 0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        ok = wait_all(&sm.kv_ready[j % kNK], (j / kNK) & 1) && (j == 0 || wait_all(&sm.s_free[T], (j - 1) & 1));
+        if (!ok) break;
+        tc::fence_after_thread_sync();
         const uint64_t dk = dk0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
         if (tc::elect_one()) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) tc::mma_e4m3(tm + kTmemS, dq + 2 * k, dk + 2 * k, idS, k > 0);
           tc::commit(smem_u32(&sm.s_full[T]));
-        }
-        __syncwarp();
-      };
-      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, &g_ctx_err));
-      };
-      bool ok = wait_all(&sm.q_ready, 0) && wait_all(&sm.kv_ready[0], 0);
-      if (ok) {
-        tc::fence_after_thread_sync();
-        issue_s(0);
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int j1 = j + 1;
-        if (j1 < n_tiles) {
-          ok = wait_all(&sm.kv_ready[j1 % kNK], (j1 / kNK) & 1) && wait_all(&sm.s_free[T], j & 1);
-          if (!ok) break;
-          tc::fence_after_thread_sync();
-          issue_s(j1);
-        }
-        ok = wait_all(&sm.p_full[T][j & 1], (j >> 1) & 1);
-        if (!ok) break;
-        tc::fence_after_thread_sync();
-        const uint32_t pa = tm + kTmemP + (uint32_t)(j & 1) * 32;
-        const uint64_t dv = dv0 + (uint64_t)((j % kNK) * ((2 * kVHalf) >> 4));
-        if (tc::elect_one()) {
-          // K = 16 keys per MMA: 8 TMEM columns of P, 16 rows (2048 B) of V
-#pragma unroll
-          for (int k = 0; k < kKT / 16; ++k)
-            tc::mma_f16_tmem_a(tm + kTmemO, pa + 8 * k, dv + 128 * k, idO, (j > 0 || k > 0) ? 1u : 0u);
-          tc::commit(smem_u32(&sm.p_free[T][j & 1]));
           tc::commit(smem_u32(&sm.kv_free[j % kNK]));
         }
         __syncwarp();
       }
-      if (tc::elect_one()) tc::commit(smem_u32(&sm.o_final[T]));
-      __syncwarp();
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ Q loader
+    // --------------------------------------------------- Q loader, PV issuer
     // One TMA box per M-tile: [32 queries][4 heads][128 d] = rows r = 4*query
     // + head, 128-byte swizzled by the tensor map.  Rows past total_q read as
     // zero; rows of the next sequence are computed but never stored.
@@ -383,6 +353,47 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       mbar_arrive_expect_tx(qb_, 2u * kQTile);
       tma_load_3d(smem_u32(sm.q[0]), &q_map, 0, g * kGroup, qo + q0, qb_);
       tma_load_3d(smem_u32(sm.q[1]), &q_map, 0, g * kGroup, qo + q0 + kQT, qb_);
+    }
+    __syncwarp();
+    // Then O_T += P_T(j) V_j for T = 0, 1 in tile order, once the softmax has
+    // written P_T(j) (p_full).  P_T(j) is in P buffer j & 1 of M-tile T; the
+    // commit on p_free tells the softmax when that buffer may take P_T(j+2)
+    // (and when O_T holds every PV up to tile j).  The V tile was published
+    // with K (kv_ready) before S_T(j); the wait below is already satisfied.
+    if (n_tiles > 0) {
+      constexpr uint32_t idO = tc::idesc_f16_f32(128, 128, true);  // B = V tile (F16), MN-major
+      const uint64_t dv0 = tc::sw128_desc_lbo(smem_u32(sm.v[0]), kVHalf);
+      const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, &g_ctx_err));
+      };
+      bool ok = true;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        ok = wait_all(&sm.kv_ready[j % kNK], (j / kNK) & 1);
+        const uint64_t dv = dv0 + (uint64_t)((j % kNK) * ((2 * kVHalf) >> 4));
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          ok = ok && wait_all(&sm.p_full[t][j & 1], (j >> 1) & 1);
+          if (!ok) break;
+          tc::fence_after_thread_sync();
+          const uint32_t tt = tm + (uint32_t)t * kTmemPerTile;
+          const uint32_t pa = tt + kTmemP + (uint32_t)(j & 1) * 32;
+          if (tc::elect_one()) {
+            // K = 16 keys per MMA: 8 TMEM columns of P, 16 rows (2048 B) of V
+#pragma unroll
+            for (int k = 0; k < kKT / 16; ++k)
+              tc::mma_f16_tmem_a(tt + kTmemO, pa + 8 * k, dv + 128 * k, idO, (j > 0 || k > 0) ? 1u : 0u);
+            tc::commit(smem_u32(&sm.p_free[t][j & 1]));
+            if (t == 1) tc::commit(smem_u32(&sm.kv_free[j % kNK]));
+          }
+          __syncwarp();
+        }
+      }
+      if (tc::elect_one()) {
+        tc::commit(smem_u32(&sm.o_final[0]));
+        tc::commit(smem_u32(&sm.o_final[1]));
+      }
+      __syncwarp();
     }
   } else if (warp < 12) {
     // -------------------------------------------------------------- softmax
