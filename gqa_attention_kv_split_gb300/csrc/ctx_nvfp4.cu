@@ -579,51 +579,70 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- dequantisers
-    // Tile j (64 keys): K then V, 512 items of (key, 16-element block) each,
-    // 4 of each per thread.  All 8 items' codes, scale bytes and scale-table
-    // entries are loaded before the wait for the K/V slot (those loads only
-    // need the packed stage), so their latencies overlap one another and the
-    // wait; K and V are then written and published together.
+    // Tile j (64 keys): K then V, each 256 items of (key, pair of adjacent
+    // 16-element blocks), 2 of each per thread: one 16-byte load of codes,
+    // one 2-byte load of scales and two scale-table entries per 32 elements.
+    // All of a tile's loads are issued before the wait for the K/V slot
+    // (they only need the packed stage), so their latencies overlap one
+    // another and the wait; K and V are then written and published together.
+    // Keys past kv_len (only in a sequence's last tile) read as zero.
     const int dt = threadIdx.x - 384;
-    const int key0 = dt >> 3;  // items dt + 128 it: key = key0 + 16 it, block = dt & 7
-    const int blk = dt & 7;
+    const int key0 = dt >> 2;  // items dt + 128 it: key = key0 + 32 it, block pair pb = dt & 3
+    const int pb = dt & 3;
+    // V: blocks 2 pb and 2 pb + 1 are d = 32 pb .. 32 pb + 31, i.e. half pb / 2,
+    // 16-byte chunks 4 (pb % 2) .. 4 (pb % 2) + 3
+    const int vc0 = 4 * (pb & 1);
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % kNP;
       const int slot = j % kNK;
       if (!mbar_wait(smem_u32(&sm.pk_full[st]), (j / kNP) & 1, &g_ctx_err)) break;
-      uint2 packed[2][4], tab[2][4];
+      uint4 packed[2][2];
+      uint2 tab[2][2][2];
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int key = key0 + 16 * it;
-          packed[kv][it] = *reinterpret_cast<const uint2*>(&sm.pk[st][kv][key * 64 + blk * 8]);
-          tab[kv][it] = sm.sftab[sm.sf[st][kv][key * 8 + blk]];
+        for (int it = 0; it < 2; ++it) {
+          const int key = key0 + 32 * it;
+          packed[kv][it] = *reinterpret_cast<const uint4*>(&sm.pk[st][kv][key * 64 + pb * 16]);
+          const uint32_t sf2 = *reinterpret_cast<const uint16_t*>(&sm.sf[st][kv][key * 8 + pb * 2]);
+          tab[kv][it][0] = sm.sftab[sf2 & 0xffu];
+          tab[kv][it][1] = sm.sftab[sf2 >> 8];
         }
       }
       if (j >= kNK && !mbar_wait(smem_u32(&sm.kv_free[slot]), ((j / kNK) - 1) & 1, &g_ctx_err)) break;
-      const bool tail = (j + 1) * kKT > kv_len;  // keys past kv_len (last tile only) read as zero
+      if ((j + 1) * kKT > kv_len) {
+        // last tile: zero the codes of keys past kv_len (code 0 dequantises to +0)
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int key = key0 + 16 * it;
-        uint4 out = dequant16_table(packed[0][it], tab[0][it]);
-        if (tail && j * kKT + key >= kv_len) out = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sm.k[slot] + swz(key, blk)) = out;
+        for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+          for (int it = 0; it < 2; ++it)
+            if (j * kKT + key0 + 32 * it >= kv_len) packed[kv][it] = make_uint4(0u, 0u, 0u, 0u);
       }
-      // V: d = 16 blk .. 16 blk + 15 -> half blk / 4, 16-byte chunks 2 (blk % 4) and 2 (blk % 4) + 1
-      uint8_t* half = sm.v[slot] + (blk >> 2) * kVHalf;
-      const int c0 = 2 * (blk & 3);
+      uint8_t* kt = sm.k[slot];
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int key = key0 + 16 * it;
-        uint4 out = dequant16_table(packed[1][it], tab[1][it]);
-        if (tail && j * kKT + key >= kv_len) out = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(half + swz(key, c0)) =
-            make_uint4(e4m3x2_to_f16x2(out.x), e4m3x2_to_f16x2(out.x >> 16), e4m3x2_to_f16x2(out.y),
-                       e4m3x2_to_f16x2(out.y >> 16));
-        *reinterpret_cast<uint4*>(half + swz(key, c0 + 1)) =
-            make_uint4(e4m3x2_to_f16x2(out.z), e4m3x2_to_f16x2(out.z >> 16), e4m3x2_to_f16x2(out.w),
-                       e4m3x2_to_f16x2(out.w >> 16));
+      for (int it = 0; it < 2; ++it) {
+        const int key = key0 + 32 * it;
+        const uint4 lo = dequant16_table(make_uint2(packed[0][it].x, packed[0][it].y), tab[0][it][0]);
+        const uint4 hi = dequant16_table(make_uint2(packed[0][it].z, packed[0][it].w), tab[0][it][1]);
+        *reinterpret_cast<uint4*>(kt + swz(key, 2 * pb)) = lo;
+        *reinterpret_cast<uint4*>(kt + swz(key, 2 * pb + 1)) = hi;
+      }
+      uint8_t* half = sm.v[slot] + (pb >> 1) * kVHalf;
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int key = key0 + 32 * it;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 e = dequant16_table(h == 0 ? make_uint2(packed[1][it].x, packed[1][it].y)
+                                                 : make_uint2(packed[1][it].z, packed[1][it].w),
+                                          tab[1][it][h]);
+          *reinterpret_cast<uint4*>(half + swz(key, vc0 + 2 * h)) =
+              make_uint4(e4m3x2_to_f16x2(e.x), e4m3x2_to_f16x2(e.x >> 16), e4m3x2_to_f16x2(e.y),
+                         e4m3x2_to_f16x2(e.y >> 16));
+          *reinterpret_cast<uint4*>(half + swz(key, vc0 + 2 * h + 1)) =
+              make_uint4(e4m3x2_to_f16x2(e.z), e4m3x2_to_f16x2(e.z >> 16), e4m3x2_to_f16x2(e.w),
+                         e4m3x2_to_f16x2(e.w >> 16));
+        }
       }
       tc::fence_proxy_async_smem();
       __syncwarp();
