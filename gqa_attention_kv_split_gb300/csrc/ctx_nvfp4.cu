@@ -192,6 +192,22 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)v));
   return d;
 }
+// 2^x on two f16 values at once (relative error below 2^-9).
+__device__ __forceinline__ uint32_t ex2_h2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t hadd2_u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Sum of the two halves of an f16x2 word, in f32.
+__device__ __forceinline__ float h2_sum_f32(uint32_t h) {
+  const __half2 v = *reinterpret_cast<const __half2*>(&h);
+  return __low2float(v) + __high2float(v);
+}
 // Two floats -> f16x2 (lo in the low half), round to nearest even.
 __device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -440,19 +456,21 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         tc::fence_after_thread_sync();
       }
       const bool mask_warp = __any_sync(0xffffffffu, masked);
-      // P = 2^(x - m_used), rounded to f16 and stored over the consumed S
-      // columns as the A operand of the F16 PV product: keys 32c..32c+31 ->
-      // columns 16c..16c+15, two keys per column.  Returns the row's sum of
-      // the unrounded P.  Masked keys (and every key of a row that has seen
-      // none) become 2^-inf = 0.  Two copies of the loop, so that the common
-      // unmasked tile carries no per-key mask test; the choice is made per
-      // warp (any lane masked): the TMEM stores are warp-collective and must
-      // not diverge.
+      // P = 2^(x - m_used) in f16 -- x = s * scale_log2 - m_used is formed in
+      // f32 and rounded to f16, then one ex2 per key pair -- written to P
+      // buffer j & 1 as the A operand of the F16 PV product: keys
+      // 32c..32c+31 -> columns 16c..16c+15, two keys per column.  Returns the
+      // row's sum of those f16 weights (a pairwise tree of f16 additions per
+      // 32 keys, then f32).  Masked keys (and every key of a row that has
+      // seen none) become 2^-inf = 0.  Two copies of the loop, so that the
+      // common unmasked tile carries no per-key mask test; the choice is made
+      // per warp (any lane masked): the TMEM stores are warp-collective and
+      // must not diverge.
       auto pass_p = [&](auto masked_tile) {
         constexpr bool kMasked = decltype(masked_tile)::value;
         const float2 cc = make_float2(scale_log2, scale_log2);
         const float2 mm = make_float2(-m_used, -m_used);
-        float2 lacc = make_float2(0.f, 0.f);
+        float lsum_c = 0.f;
 #pragma unroll
         for (int c = 0; c < kKT / 32; ++c) {
           const uint32_t* v = c == 0 ? v0 : v1;
@@ -465,17 +483,23 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
               if (k0 > lim) x.x = -INFINITY;
               if (k0 + 1 > lim) x.y = -INFINITY;
             }
-            const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-            lacc = __fadd2_rn(lacc, pr);
-            pp[q] = f2_to_h2(pr.x, pr.y);
+            pp[q] = ex2_h2(f2_to_h2(x.x, x.y));
           }
           tc::st16(tP + 16 * c, pp);
+          uint32_t t8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t8[i] = hadd2_u(pp[2 * i], pp[2 * i + 1]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) t8[i] = hadd2_u(t8[2 * i], t8[2 * i + 1]);
+          t8[0] = hadd2_u(hadd2_u(t8[0], t8[1]), hadd2_u(t8[2], t8[3]));
+          lsum_c += h2_sum_f32(t8[0]);
         }
-        return lacc.x + lacc.y;
+        return lsum_c;
       };
       // Optimistic pass with the running maximum as it stands.  A row sum of
-      // at most 2^15 bounds every P of the row by 2^15 < 65504, so the f16
-      // values are finite and the tile is done.  Otherwise (a row's first
+      // at most 2^15 bounds every P of the row by about 2^15 < 65504, so the
+      // f16 values are finite and the tile is done (an overflowing weight or
+      // partial sum is inf and fails the test).  Otherwise (a row's first
       // keys, where m_used is -inf, or a maximum that grew by more than ~9) the
       // warp finds the rows' maxima, raises m where it grew by more than
       // 2^kRescaleLog2 (rescaling O and l), and computes P again.
