@@ -219,6 +219,9 @@ DECODE_WORKLOADS = {
 CTX_WORKLOADS = {
     "ctx_b4_q2048_kv2048": dict(q_lens=[2048] * 4, kv_lens=[2048] * 4, seed=3),
     "ctx_b2_q4096_kv65536": dict(q_lens=[4096] * 2, kv_lens=[65536] * 2, seed=4),
+    # profiling case: one wave of 128 long units (1024 queries x 8 KV heads over 16384 keys), so that
+    # counters show the steady state without per-unit start-up; not a benchmark configuration
+    "ctx_b1_q1024_kv16384": dict(q_lens=[1024], kv_lens=[16384], seed=7),
 }
 
 
