@@ -43,6 +43,10 @@ constexpr int kThreads = (kComputeWarps + 1) * 32;    // + one producer warp
 constexpr int kRowBytes = kD * 2;                     // one token of one head: 256 B
 constexpr int kStageBytes = kStageTok * kRowBytes;    // 4 KB of K (and of V)
 constexpr int kChunkQuantum = kStageTok * kComputeWarps;  // 64 tokens
+// Consumer warp w takes ring positions w, w + kComputeWarps, ...; with a ring
+// depth that is a multiple of the warp count every stage belongs to one warp,
+// so no warp can wait on a stage's barrier a phase ahead of the data.
+static_assert(kStages % kComputeWarps == 0, "each ring stage must be owned by one consumer warp");
 
 __device__ uint32_t g_decode_err;
 
@@ -67,7 +71,7 @@ __device__ __forceinline__ void h8_to_f8(const uint4& u, float f[8]) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __half* __restrict__ q, const __half* __restrict__ kv,
                         const int32_t* __restrict__ seq_lens, float* __restrict__ part_o,
                         float2* __restrict__ part_ml, __half* __restrict__ out, int64_t cap, int chunk,
