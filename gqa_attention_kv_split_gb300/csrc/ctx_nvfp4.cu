@@ -14,12 +14,13 @@
 //    heads of the group are stacked into the MMA's M dimension: M-tile T
 //    (T = 0, 1) holds queries 32T..32T+31 of the block x 4 heads, row
 //    r = 4 * query + head.  One dequantised K/V tile therefore feeds 256 rows.
-//  * KV tiles of 64 keys (one page).  TMEM (512 columns) per M-tile T: S (64
-//    fp32 columns), two P buffers (32 columns each: 64 f16 weights per row)
-//    and O (128 columns).  S of tile j+1 is computed as soon as the softmax
-//    has read S of tile j into registers, i.e. while the softmax works on
-//    tile j; P of tile j goes to P buffer j & 1 and is read from TMEM as the
-//    A operand of PV.
+//  * KV tiles of 64 keys (one page).  TMEM (512 columns) per M-tile T: two
+//    S buffers (64 fp32 columns each, tile j in buffer j & 1) and O (128
+//    columns).  The softmax writes P of tile j (64 f16 weights per row = 32
+//    columns) over the first half of the S buffer it read, and PV reads it
+//    there as its TMEM A operand.  So S of tile j+1 is computed into the
+//    other buffer while the softmax works on tile j; S of tile j+2 waits
+//    only for the PV of tile j, the last reader of its buffer.
 //  * Warp roles (16 warps): 0 = bulk-copy producer of packed NVFP4 pages +
 //    scales through the block table into a 6-stage ring; 1 and 3 = issuers
 //    of S = Q K^T for M-tile 0 and 1 (warp 1 also owns the TMEM allocation);
@@ -29,10 +30,10 @@
 //    writing the K tile (E4M3) and the V tile (its E4M3 values widened to
 //    F16) in the 128-byte swizzled layouts the MMA descriptors read (K as the
 //    K-major B operand of S = Q K^T, V as the MN-major B operand of O = P V).
-//  * Per M-tile T and KV tile j: S_T(j+1) is issued once the softmax has read
-//    S_T(j); PV_T(j) once it has written P_T(j).  A softmax warp that raises
-//    its running maximum waits for the PV of the previous tile before
-//    rescaling O in TMEM.
+//  * Per M-tile T and KV tile j: S_T(j) is issued once K of tile j is
+//    dequantised and PV_T(j-2) has completed; PV_T(j) once the softmax has
+//    written P_T(j).  A softmax warp that raises its running maximum waits
+//    for the PV of the previous tile before rescaling O in TMEM.
 //  * Online softmax in the exp2 domain with a lazy running maximum m: m is
 //    raised only when a row's maximum exceeds it by more than 2^8, so O is
 //    rescaled rarely.
@@ -109,11 +110,11 @@ constexpr int kScalePage = kPage * kD / 16;   // 512 B of scales per (page, KV h
 constexpr float kRescaleLog2 = 8.f;        // lazy-maximum threshold when a row's maximum is recomputed
 constexpr float kMaxTileSum = 32768.f;     // a tile's row sum of P up to which no P can overflow f16
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns of M-tile T, from T*256: S (64 f32 columns), two P buffers
-// (32 columns of f16 pairs each, tile j in buffer j & 1), O (128 columns).
+// TMEM columns of M-tile T, from T*256: two S/P buffers (64 f32 columns of S
+// each, tile j in buffer j & 1; P of the tile, as f16 pairs, overwrites the
+// buffer's first 32 columns), O (128 columns).
 constexpr uint32_t kTmemPerTile = 256;
-constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemP = 64;
+constexpr uint32_t kTmemSP = 64;  // columns per S/P buffer
 constexpr uint32_t kTmemO = 128;
 
 struct CtxSmem {
@@ -124,8 +125,8 @@ struct CtxSmem {
   uint8_t sf[kNP][2][kScalePage];   // [stage][K,V][slot*8 + block]
   uint64_t pk_full[kNP], pk_empty[kNP];
   uint64_t kv_ready[kNK], kv_free[kNK];  // dequantised K and V tile of a slot written / slot consumed
-  uint64_t s_full[2], s_free[2];        // [M-tile]: S computed / S read by the 4 softmax warps
-  uint64_t p_full[2][2], p_free[2][2];  // [M-tile][P buffer]: P written / the PV that read it completed
+  uint64_t s_full[2][2];                // [M-tile][buffer]: S computed
+  uint64_t p_full[2][2], p_free[2][2];  // [M-tile][buffer]: P written / the PV that read it completed
   uint64_t o_final[2], q_ready;  // o_final: every MMA of an M-tile completed
   uint2 sftab[256];      // E4M3 magnitudes of the 8 E2M1 codes for every scale byte
   uint32_t tmem_base;
@@ -266,9 +267,8 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       mbar_init(smem_u32(&sm.kv_free[i]), 3);  // S of both M-tiles, PV of both
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&sm.s_full[t]), 1);
-      mbar_init(smem_u32(&sm.s_free[t]), 4);
       for (int i = 0; i < 2; ++i) {
+        mbar_init(smem_u32(&sm.s_full[t][i]), 1);
         mbar_init(smem_u32(&sm.p_full[t][i]), 4);
         mbar_init(smem_u32(&sm.p_free[t][i]), 1);
       }
@@ -327,9 +327,11 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
   } else if (warp == 1 || warp == 3) {
     // -------------------------------------------------------- S issuers
     // Warp 1 issues S = Q K^T of M-tile 0, warp 3 that of M-tile 1: S_T(j)
-    // once K of tile j is dequantised and the softmax has read S_T(j-1) into
-    // registers (s_free), so S of the next tile is computed while the
-    // softmax works on this one.  tcgen05.mma issue blocks while the tensor
+    // into buffer j & 1 once K of tile j is dequantised and PV_T(j-2), which
+    // read P_T(j-2) from that buffer, has completed (p_free), so S of the
+    // next tile is computed while the softmax works on this one.  Waiting
+    // for that PV also orders this S after the softmax's reads of S_T(j-2)
+    // and its writes of P_T(j-2).  tcgen05.mma issue blocks while the tensor
     // pipe is busy, so S and PV have separate issuing warps and an S is
     // never queued behind a PV the softmax is not waiting for.  The whole
     // warp runs this code (descriptor arithmetic stays warp-uniform, which
@@ -346,14 +348,16 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       };
       bool ok = wait_all(&sm.q_ready, 0);
       for (int j = 0; ok && j < n_tiles; ++j) {
-        ok = wait_all(&sm.kv_ready[j % kNK], (j / kNK) & 1) && (j == 0 || wait_all(&sm.s_free[T], (j - 1) & 1));
+        ok = wait_all(&sm.kv_ready[j % kNK], (j / kNK) & 1) &&
+             (j < 2 || wait_all(&sm.p_free[T][j & 1], ((j >> 1) - 1) & 1));
         if (!ok) break;
         tc::fence_after_thread_sync();
         const uint64_t dk = dk0 + (uint64_t)((j % kNK) * (kKVTile >> 4));
+        const uint32_t ts = tm + (uint32_t)(j & 1) * kTmemSP;
         if (tc::elect_one()) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tc::mma_e4m3(tm + kTmemS, dq + 2 * k, dk + 2 * k, idS, k > 0);
-          tc::commit(smem_u32(&sm.s_full[T]));
+          for (int k = 0; k < 4; ++k) tc::mma_e4m3(ts, dq + 2 * k, dk + 2 * k, idS, k > 0);
+          tc::commit(smem_u32(&sm.s_full[T][j & 1]));
           tc::commit(smem_u32(&sm.kv_free[j % kNK]));
         }
         __syncwarp();
@@ -372,9 +376,9 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     }
     __syncwarp();
     // Then O_T += P_T(j) V_j for T = 0, 1 in tile order, once the softmax has
-    // written P_T(j) (p_full).  P_T(j) is in P buffer j & 1 of M-tile T; the
-    // commit on p_free tells the softmax when that buffer may take P_T(j+2)
-    // (and when O_T holds every PV up to tile j).  The V tile was published
+    // written P_T(j) (p_full).  P_T(j) is in buffer j & 1 of M-tile T; the
+    // commit on p_free tells the S issuer when that buffer may take S_T(j+2)
+    // (and the softmax when O_T holds every PV up to tile j).  The V tile was published
     // with K (kv_ready) before S_T(j); the wait below is already satisfied.
     if (n_tiles > 0) {
       constexpr uint32_t idO = tc::idesc_f16_f32(128, 128, true);  // B = V tile (F16), MN-major
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
           if (!ok) break;
           tc::fence_after_thread_sync();
           const uint32_t tt = tm + (uint32_t)t * kTmemPerTile;
-          const uint32_t pa = tt + kTmemP + (uint32_t)(j & 1) * 32;
+          const uint32_t pa = tt + (uint32_t)(j & 1) * kTmemSP;
           if (tc::elect_one()) {
             // K = 16 keys per MMA: 8 TMEM columns of P, 16 rows (2048 B) of V
 #pragma unroll
@@ -422,7 +426,6 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     if (lim > kv_len - 1) lim = kv_len - 1;
     const uint32_t lane_off = (uint32_t)(32 * sub) << 16;
     const uint32_t tT = tmem + lane_off + (uint32_t)T * kTmemPerTile;
-    const uint32_t tS = tT + kTmemS;
     const uint32_t tO = tT + kTmemO;
     float m_used = -INFINITY;
     float l = 0.f;
@@ -430,34 +433,26 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     const bool neg_scale = scale_log2 < 0.f;
     for (int j = 0; j < n_tiles; ++j) {
       // warp-uniform outcome: the TMEM accesses below are warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[T]), j & 1, &g_ctx_err))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[T][j & 1]), (j >> 1) & 1, &g_ctx_err))) {
         ok = false;
         break;
       }
       tc::fence_after_thread_sync();
-      const uint32_t tP = tT + kTmemP + (uint32_t)(j & 1) * 32;
+      // buffer j & 1: S of the tile, then P over its first 32 columns (the
+      // PV that read the buffer's previous P completed before this S was
+      // issued)
+      const uint32_t tS = tT + (uint32_t)(j & 1) * kTmemSP;
+      const uint32_t tP = tS;
       const int kbase = j * kKT;
       const bool masked = kbase + kKT - 1 > lim;
-      // the tile's 64 logits stay in registers; once all four warps have
-      // read them the issuer may compute S of the next tile in their place
+      // the tile's 64 logits stay in registers while P is written in their place
       uint32_t v0[32], v1[32];
       tc::ld32(tS, v0);
       tc::ld32(tS + 32, v1);
       tc::ld_wait();
-      tc::fence_before_thread_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.s_free[T]));
-      // P buffer j & 1 was last read by PV of tile j - 2
-      if (j >= 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_free[T][j & 1]), ((j >> 1) - 1) & 1, &g_ctx_err))) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_thread_sync();
-      }
       const bool mask_warp = __any_sync(0xffffffffu, masked);
       // P = 2^(x - m_used) in f16 -- x = s * scale_log2 - m_used is formed in
-      // f32 and rounded to f16, then one ex2 per key pair -- written to P
+      // f32 and rounded to f16, then one ex2 per key pair -- written to
       // buffer j & 1 as the A operand of the F16 PV product: keys
       // 32c..32c+31 -> columns 16c..16c+15, two keys per column.  Returns the
       // row's sum of those f16 weights (a pairwise tree of f16 additions per

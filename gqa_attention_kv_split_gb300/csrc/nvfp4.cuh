@@ -1,7 +1,7 @@
 // nvfp4.cuh -- NVFP4 (E2M1 codes + E4M3 block scale) -> E4M3 dequantisation
-// on sm_103a, the step "dequantise the NVFP4 K/V page to E4M3 in shared
-// memory" of "GB300 NVFP4 Context Attention: scale slot 조기 반납과 8단 packed
-// K/V ring" (introduction).
+// on sm_103a: the conversion of packed K/V pages to E4M3 tiles in shared
+// memory that the context attention of "GB300 NVFP4 Context Attention: scale
+// slot 조기 반납과 8단 packed K/V ring" (introduction) performs.
 //
 // value = E4M3_rne_satfinite( e2m1(code) * e4m3(scale) ).
 // The product is formed in f16, where it is exact: an E2M1 value has at most
@@ -16,13 +16,6 @@
 
 namespace gqa {
 
-// Two E2M1 codes (one byte; element 2i in the low nibble) -> f16x2 with the
-// low nibble in the low half.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
-  return r;
-}
 
 // E4M3 scale byte -> f16x2 (s, s).
 __device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t sf) {

@@ -94,17 +94,6 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T: A (M=128 rows, one per TMEM lane) read
-// from 8 TMEM columns holding 32 8-bit K elements per row, 4 per column.
-__device__ __forceinline__ void mma_e4m3_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: one K=16 step of F16
 // operands, A read from 8 TMEM columns holding 2 elements per column
