@@ -304,24 +304,38 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // One page per KV tile: packed K and V codes (4 KB each) and their scales
-    // (512 B each) through the block table.
-    if (lane == 0 && n_tiles > 0) {
+    // (512 B each) through the block table.  The page numbers are read 32 at
+    // a time by the whole warp, one chunk ahead of use, so no copy waits for
+    // a block-table read; lane 0 issues the copies.
+    if (n_tiles > 0) {
       const uint64_t pol = policy_evict_last();  // pages are re-read by the other query blocks
+      const int32_t* bt = a.block_table + (int64_t)b * a.max_pages_per_seq;
+      int cur = lane < n_tiles ? bt[lane] : 0;
+      int nxt = 32 + lane < n_tiles ? bt[32 + lane] : 0;
       for (int j = 0; j < n_tiles; ++j) {
-        const int st = j % kNP;
-        if (j >= kNP && !mbar_wait(smem_u32(&sm.pk_empty[st]), ((j / kNP) - 1) & 1, &g_ctx_err)) break;
-        int phys = a.block_table[(int64_t)b * a.max_pages_per_seq + j];
-        if (phys < 0 || phys >= a.num_pages) {
-          atomicOr(&g_ctx_err, kErrBadIndex);
-          phys = 0;
+        if (j > 0 && (j & 31) == 0) {
+          cur = nxt;
+          nxt = j + 32 + lane < n_tiles ? bt[j + 32 + lane] : 0;
         }
-        const int64_t row = ((int64_t)phys * kHkv + g) * kPage;
-        const uint32_t fb = smem_u32(&sm.pk_full[st]);
-        mbar_arrive_expect_tx(fb, 2u * (kPackedPage + kScalePage));
-        bulk_g2s_hint(smem_u32(sm.pk[st][0]), a.k_fp4 + row * (kD / 2), kPackedPage, fb, pol);
-        bulk_g2s_hint(smem_u32(sm.sf[st][0]), a.k_sf + row * (kD / 16), kScalePage, fb, pol);
-        bulk_g2s_hint(smem_u32(sm.pk[st][1]), a.v_fp4 + row * (kD / 2), kPackedPage, fb, pol);
-        bulk_g2s_hint(smem_u32(sm.sf[st][1]), a.v_sf + row * (kD / 16), kScalePage, fb, pol);
+        int phys = __shfl_sync(0xffffffffu, cur, j & 31);
+        const int st = j % kNP;
+        if (j >= kNP &&
+            !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.pk_empty[st]), ((j / kNP) - 1) & 1, &g_ctx_err)))
+          break;
+        if (lane == 0) {
+          if (phys < 0 || phys >= a.num_pages) {
+            atomicOr(&g_ctx_err, kErrBadIndex);
+            phys = 0;
+          }
+          const int64_t row = ((int64_t)phys * kHkv + g) * kPage;
+          const uint32_t fb = smem_u32(&sm.pk_full[st]);
+          mbar_arrive_expect_tx(fb, 2u * (kPackedPage + kScalePage));
+          bulk_g2s_hint(smem_u32(sm.pk[st][0]), a.k_fp4 + row * (kD / 2), kPackedPage, fb, pol);
+          bulk_g2s_hint(smem_u32(sm.sf[st][0]), a.k_sf + row * (kD / 16), kScalePage, fb, pol);
+          bulk_g2s_hint(smem_u32(sm.pk[st][1]), a.v_fp4 + row * (kD / 2), kPackedPage, fb, pol);
+          bulk_g2s_hint(smem_u32(sm.sf[st][1]), a.v_sf + row * (kD / 16), kScalePage, fb, pol);
+        }
+        __syncwarp();
       }
     }
   } else if (warp == 1 || warp == 3) {
