@@ -41,6 +41,10 @@ if ROOT not in sys.path:
 METRIC = "GQA decode HBM GB/s (% of GB300 peak); NVFP4 ctx attn TFLOP/s (% FP8 peak)"
 DECODE_WL = "decode_b64_cap8192"
 CTX_WL = "ctx_b4_q2048_kv2048"
+# Latency-bound rows of the results table of "GB300 NVFP4 Context Attention: scale slot 조기 반납과 8단
+# packed K/V ring" (GB300, its kernel after the change), read as batch x q_len x kv_len: context for the
+# workloads of the same shape, not a target of this metric.
+PAGE_ROWS_US = {"ctx_b2_q1_kv4096": ("2 x 1 x 4096", 44.5), "ctx_b1_q32_kv32768": ("1 x 32 x 32768", 329.8)}
 FALLBACK_HBM = 6800.0
 FALLBACK_BF16 = 1900.0
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
@@ -293,6 +297,9 @@ def run_gpu(args):
     clocks = clk.summary()
     line = {"metric": METRIC}
     n_launch_dec = gqa.gqa_decode_plan(dx.batch, dx.capacity)["num_launches"] if dx is not None else 0
+    ctx_plan = (gqa.gqa_ctx_plan(cx.block_table.shape[0], cx.q_fp8.shape[0], cx.block_table.shape[1])
+                if cx is not None else None)
+    n_launch_ctx = ctx_plan["num_launches"] if (ctx_plan is not None and ctx_ok) else 0
     if dx is not None:
         gbs = dx.kv_bytes_read() * world / (dec_max * 1e-3) / 1e9
         traffic = profiled_traffic("decode_split_kernel_decode_b64_cap8192.md", ["decode.cu", "common.cuh"])
@@ -318,13 +325,18 @@ def run_gpu(args):
             flops = cx.causal_flops()
             tf = flops / (ctx_max * 1e-3) / 1e12
             fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+            # the committed counters were taken on ctx_b4_q2048_kv2048 only
+            traffic_c = (profiled_traffic("ctx_nvfp4_kernel_ctx_b4_q2048_kv2048.md",
+                                          ["ctx_nvfp4.cu", "common.cuh", "nvfp4.cuh"])
+                         if ctx_name == CTX_WL else None)
             ctx_obj = {"value": round(tf * world, 2), "unit": "TFLOP/s", "ms": round(ctx_max, 4),
-                       "causal_flops_per_step": flops, "workload": ctx_name, "dtype": "e4m3",
+                       "causal_flops_per_step": flops, "workload": ctx_name, "dtype": "e4m3", "plan": ctx_plan,
                        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": round(fp8_peak, 1),
-                                    "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4),
-                                    "traffic": profiled_traffic("ctx_nvfp4_kernel_ctx_b4_q2048_kv2048.md",
-                                                                ["ctx_nvfp4.cu", "common.cuh", "nvfp4.cuh"]),
+                                    "unit": "TFLOP/s", "frac": round(tf / fp8_peak, 4), "traffic": traffic_c,
                                     "peak_source": f"{peaks['source']} bf16 x {FP8_OVER_BF16} (nominal FP8:bf16)"}}
+            if ctx_name in PAGE_ROWS_US:
+                label, us = PAGE_ROWS_US[ctx_name]
+                ctx_obj["page_row"] = {"label": label, "us": us, "ours_us": round(ctx_max * 1e3, 2)}
         else:
             ctx_obj = {"unavailable": ctx_err or "not run"}
     if dx is None and ctx_ok:
@@ -337,7 +349,7 @@ def run_gpu(args):
     if ctx_obj is not None:
         line["ctx_attn"] = ctx_obj
     line["e2e"] = e2e
-    line["gpu_launches"] = args.steps * (n_launch_dec + (1 if ctx_ok else 0))
+    line["gpu_launches"] = args.steps * (n_launch_dec + n_launch_ctx)
     line["clocks"] = clocks
     line["wall_s_timed_region"] = round(wall, 4)
     if args.cpu_baseline and dx is not None:

@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "GqaError", "lib", "gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages",
-    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_decode_noalloc", "LIB_PATH",
+    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_noalloc", "LIB_PATH",
     "build",
 ]
 
@@ -76,6 +76,9 @@ def lib() -> ctypes.CDLL:
             L.gqa_decode_plan.argtypes = [i64, i64, c.POINTER(c.c_int32), c.POINTER(c.c_int32),
                                           c.POINTER(c.c_int32)]
             L.gqa_decode_plan.restype = c.c_int
+            L.gqa_ctx_plan.argtypes = [i64, i64, i64, c.POINTER(c.c_int32), c.POINTER(c.c_int32),
+                                       c.POINTER(c.c_int32)]
+            L.gqa_ctx_plan.restype = c.c_int
             L.gqa_release_workspace.argtypes = []
             L.gqa_release_workspace.restype = c.c_int
             _lib = L
@@ -198,6 +201,14 @@ def gqa_decode_plan(batch: int, capacity: int) -> dict:
     t, n, l = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     _check(lib().gqa_decode_plan(int(batch), int(capacity), ctypes.byref(t), ctypes.byref(n), ctypes.byref(l)))
     return {"tokens_per_split": t.value, "num_splits": n.value, "num_launches": l.value}
+
+
+def gqa_ctx_plan(batch: int, total_q: int, max_pages_per_seq: int) -> dict:
+    """tiles_per_split, num_splits and num_launches of an nvfp4_paged_ctx_attn call."""
+    t, n, l = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().gqa_ctx_plan(int(batch), int(total_q), int(max_pages_per_seq), ctypes.byref(t), ctypes.byref(n),
+                              ctypes.byref(l)))
+    return {"tiles_per_split": t.value, "num_splits": n.value, "num_launches": l.value}
 
 
 def gqa_check_device_errors(device: int = 0) -> int:

@@ -277,6 +277,19 @@ gqa_status gqa_decode_plan(int64_t batch, int64_t capacity, int32_t* tokens_per_
   return GQA_OK;
 }
 
+gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_seq, int32_t* tiles_per_split,
+                        int32_t* num_splits, int32_t* num_launches) {
+  if (batch < 1 || batch > (1 << 20)) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 2^20]", (long long)batch);
+  if (total_q < 0 || total_q > 2147483647LL) return fail(GQA_ERR_INVALID_ARG, "total_q %lld out of range", (long long)total_q);
+  if (max_pages_per_seq < 1 || max_pages_per_seq > (2147483647LL / 64))
+    return fail(GQA_ERR_INVALID_ARG, "max_pages_per_seq %lld out of range", (long long)max_pages_per_seq);
+  const gqa::CtxPlan plan = gqa::plan_ctx(batch, total_q, max_pages_per_seq);
+  if (tiles_per_split) *tiles_per_split = plan.tiles_per_split;
+  if (num_splits) *num_splits = plan.n_splits;
+  if (num_launches) *num_launches = total_q == 0 ? 0 : (plan.n_splits > 1 ? 2 : 1);
+  return GQA_OK;
+}
+
 gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_fp4, const void* k_sf,
                                 const void* v_fp4, const void* v_sf, const int32_t* block_table,
                                 const int32_t* qo_indptr, const int32_t* kv_lens, void* out_fp8,
@@ -311,11 +324,15 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
   a.total_q = total_q;
   a.num_pages = num_pages;
   a.max_pages_per_seq = max_pages_per_seq;
+  const gqa::CtxPlan plan = gqa::plan_ctx(batch, total_q, max_pages_per_seq);
+  const size_t part_bytes = gqa::ctx_workspace_bytes(total_q, plan);
 
   if (!where.host) {
     if (total_q == 0) return GQA_OK;
     ScopedDevice sd(where.device);
     if (!sd.ok()) return fail(GQA_ERR_CUDA, "cannot switch to device %d", where.device);
+    void* part = nullptr;
+    if (part_bytes && (st = workspace(where.device, stream, part_bytes, &part)) != GQA_OK) return st;
     a.q = static_cast<const uint8_t*>(q_fp8);
     a.k_fp4 = static_cast<const uint8_t*>(k_fp4);
     a.k_sf = static_cast<const uint8_t*>(k_sf);
@@ -325,7 +342,7 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
     a.qo_indptr = qo_indptr;
     a.kv_lens = kv_lens;
     a.out = static_cast<uint8_t*>(out_fp8);
-    cudaError_t e = gqa::launch_ctx(a, stream);
+    cudaError_t e = gqa::launch_ctx(a, plan, part, stream);
     if (e == cudaErrorNotSupported) return fail(GQA_ERR_UNSUPPORTED, "context kernel not available in this build");
     GQA_CUDA_TRY(e, "ctx launch");
     return GQA_OK;
@@ -356,7 +373,7 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
   Carver c;
   const size_t o_q = c.take(q_bytes), o_kf = c.take(fp4_bytes), o_ks = c.take(sf_bytes), o_vf = c.take(fp4_bytes),
                o_vs = c.take(sf_bytes), o_bt = c.take(bt_bytes), o_qi = c.take((size_t)(batch + 1) * 4),
-               o_kl = c.take((size_t)batch * 4), o_out = c.take(q_bytes);
+               o_kl = c.take((size_t)batch * 4), o_out = c.take(q_bytes), o_part = c.take(part_bytes);
   void* ws = nullptr;
   if ((st = workspace(dev, stream, c.off, &ws)) != GQA_OK) return st;
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -376,7 +393,7 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
   a.qo_indptr = reinterpret_cast<const int32_t*>(base + o_qi);
   a.kv_lens = reinterpret_cast<const int32_t*>(base + o_kl);
   a.out = base + o_out;
-  cudaError_t e = gqa::launch_ctx(a, stream);
+  cudaError_t e = gqa::launch_ctx(a, plan, part_bytes ? base + o_part : nullptr, stream);
   if (e == cudaErrorNotSupported) return fail(GQA_ERR_UNSUPPORTED, "context kernel not available in this build");
   GQA_CUDA_TRY(e, "ctx launch");
   GQA_CUDA_TRY(cudaMemcpyAsync(out_fp8, base + o_out, q_bytes, cudaMemcpyDeviceToHost, stream), "copy out");

@@ -239,9 +239,11 @@ __device__ __forceinline__ uint32_t f4_to_e4m3x4(float e0, float e1, float e2, f
   return r;
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kCtxThreads, 1)
     ctx_nvfp4_kernel(const CtxArgs a, const __grid_constant__ CUtensorMap q_map, const float scale_log2,
-                     const float inv_out_scale) {
+                     const float inv_out_scale, const int tiles_per_split, float* __restrict__ part_o,
+                     float2* __restrict__ part_ml) {
   extern __shared__ uint8_t smem_raw[];
   CtxSmem& sm = *reinterpret_cast<CtxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -290,7 +292,17 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
   const int q0 = qb * kQB;
   const int q_last = min(q0 + kQB, q_len) - 1;
   const int n_keys = min(kv_len, kv_len - q_len + q_last + 1);
-  const int n_tiles = n_keys > 0 ? (n_keys + kKT - 1) / kKT : 0;
+  const int unit_tiles = n_keys > 0 ? (n_keys + kKT - 1) / kKT : 0;
+  // Split-KV (kSplit): this CTA takes the unit's tiles
+  // [t_begin, t_begin + tiles_per_split) and writes partial results.  Loop
+  // indices j below are local (tile t_begin + j); the ring and barrier
+  // phases count local tiles.
+  const int t_begin = kSplit ? (int)blockIdx.y * tiles_per_split : 0;
+  const int n_tiles = kSplit ? max(0, min(unit_tiles - t_begin, tiles_per_split)) : unit_tiles;
+  // M-tile 1 holds queries q0 + 32 .. q0 + 63; when none of them exists (a
+  // sequence's last block of at most 32 queries) it is not computed: its S
+  // issuer only releases the K/V slots and its softmax warps stay idle.
+  const bool t1_live = q0 + kQT < q_len;
 
   if (warp == 1) {
     tc::tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
@@ -309,7 +321,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     // a block-table read; lane 0 issues the copies.
     if (n_tiles > 0) {
       const uint64_t pol = policy_evict_last();  // pages are re-read by the other query blocks
-      const int32_t* bt = a.block_table + (int64_t)b * a.max_pages_per_seq;
+      const int32_t* bt = a.block_table + (int64_t)b * a.max_pages_per_seq + t_begin;
       int cur = lane < n_tiles ? bt[lane] : 0;
       int nxt = 32 + lane < n_tiles ? bt[32 + lane] : 0;
       for (int j = 0; j < n_tiles; ++j) {
@@ -361,6 +373,13 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, &g_ctx_err));
       };
       bool ok = wait_all(&sm.q_ready, 0);
+      if (T == 1 && !t1_live) {
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          ok = wait_all(&sm.kv_ready[j % kNK], (j / kNK) & 1);
+          if (ok && lane == 0) mbar_arrive(smem_u32(&sm.kv_free[j % kNK]));
+        }
+        ok = false;  // nothing to issue
+      }
       for (int j = 0; ok && j < n_tiles; ++j) {
         ok = wait_all(&sm.kv_ready[j % kNK], (j / kNK) & 1) &&
              (j < 2 || wait_all(&sm.p_free[T][j & 1], ((j >> 1) - 1) & 1));
@@ -402,11 +421,13 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         return __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, &g_ctx_err));
       };
       bool ok = true;
+      const int n_mt = t1_live ? 2 : 1;  // M-tiles computed
       for (int j = 0; ok && j < n_tiles; ++j) {
         ok = wait_all(&sm.kv_ready[j % kNK], (j / kNK) & 1);
         const uint64_t dv = dv0 + (uint64_t)((j % kNK) * ((2 * kVHalf) >> 4));
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
+          if (t >= n_mt) break;
           ok = ok && wait_all(&sm.p_full[t][j & 1], (j >> 1) & 1);
           if (!ok) break;
           tc::fence_after_thread_sync();
@@ -418,7 +439,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
             for (int k = 0; k < kKT / 16; ++k)
               tc::mma_f16_tmem_a(tt + kTmemO, pa + 8 * k, dv + 128 * k, idO, (j > 0 || k > 0) ? 1u : 0u);
             tc::commit(smem_u32(&sm.p_free[t][j & 1]));
-            if (t == 1) tc::commit(smem_u32(&sm.kv_free[j % kNK]));
+            if (t == n_mt - 1) tc::commit(smem_u32(&sm.kv_free[j % kNK]));
           }
           __syncwarp();
         }
@@ -445,7 +466,8 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     float l = 0.f;
     bool ok = true;
     const bool neg_scale = scale_log2 < 0.f;
-    for (int j = 0; j < n_tiles; ++j) {
+    const int n_mine = (T == 1 && !t1_live) ? 0 : n_tiles;  // tiles this M-tile computes
+    for (int j = 0; j < n_mine; ++j) {
       // warp-uniform outcome: the TMEM accesses below are warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[T][j & 1]), (j >> 1) & 1, &g_ctx_err))) {
         ok = false;
@@ -457,7 +479,7 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
       // issued)
       const uint32_t tS = tT + (uint32_t)(j & 1) * kTmemSP;
       const uint32_t tP = tS;
-      const int kbase = j * kKT;
+      const int kbase = (t_begin + j) * kKT;
       const bool masked = kbase + kKT - 1 > lim;
       // the tile's 64 logits stay in registers while P is written in their place
       uint32_t v0[32], v1[32];
@@ -580,15 +602,39 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
     }
     // ------------------------------------------------------------ epilogue
     bool have_o = false;
-    if (ok && n_tiles > 0) {
+    if (ok && n_mine > 0) {
       have_o = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_final[T]), 0, &g_ctx_err));
       tc::fence_after_thread_sync();
     }
+    const bool store = qrow < q_len;
+    if constexpr (kSplit) {
+      // Split-KV: this range's unnormalised O and its (m, l), in the exp2
+      // domain of the scaled logits: O = sum 2^(x - m) V, l = sum 2^(x - m).
+      // A range in which the row sees no key leaves l = 0.
+      const int64_t prow = ((int64_t)blockIdx.y * a.total_q + qo + qrow) * kHq + g * kGroup + hh;
+      float4* po = reinterpret_cast<float4*>(part_o + prow * kD);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        if (have_o) {
+          tc::ld32(tO + 32 * c, o);
+          tc::ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        if (store) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            po[8 * c + i] = make_float4(u2f(o[4 * i]), u2f(o[4 * i + 1]), u2f(o[4 * i + 2]), u2f(o[4 * i + 3]));
+        }
+      }
+      if (store) part_ml[prow] = make_float2(have_o ? m_used : -INFINITY, have_o ? l : 0.f);
+    }
     const float inv = (l > 0.f) ? inv_out_scale / l : 0.f;
     uint8_t* dst = a.out + ((int64_t)(qo + qrow) * kHq + g * kGroup + hh) * kD;
-    const bool store = qrow < q_len;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; !kSplit && c < 4; ++c) {
       uint32_t o[32];
       if (have_o) {
         tc::ld32(tO + 32 * c, o);
@@ -643,13 +689,13 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
         }
       }
       if (j >= kNK && !mbar_wait(smem_u32(&sm.kv_free[slot]), ((j / kNK) - 1) & 1, &g_ctx_err)) break;
-      if ((j + 1) * kKT > kv_len) {
+      if ((t_begin + j + 1) * kKT > kv_len) {
         // last tile: zero the codes of keys past kv_len (code 0 dequantises to +0)
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv)
 #pragma unroll
           for (int it = 0; it < 2; ++it)
-            if (j * kKT + key0 + 32 * it >= kv_len) packed[kv][it] = make_uint4(0u, 0u, 0u, 0u);
+            if ((t_begin + j) * kKT + key0 + 32 * it >= kv_len) packed[kv][it] = make_uint4(0u, 0u, 0u, 0u);
       }
       uint8_t* kt = sm.k[slot];
 #pragma unroll
@@ -695,13 +741,56 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Split-KV merge: one warp per (query row, head), lane l holding head-dim
+// elements 4l .. 4l+3.  With M the largest m of the ranges that saw a key,
+//   out = E4M3( sum_s 2^(m_s - M) O_s / (sum_s 2^(m_s - M) l_s) / out_scale ),
+// and zeros when no range saw one (the same result as one unsplit pass, up
+// to f32 rounding order).
+// ---------------------------------------------------------------------------
+constexpr int kMergeWarps = 8;
+constexpr int kCtxSplitTargetCtas = 152;  // one wave: one CTA per SM
+constexpr int kMinTilesPerSplit = 8;      // a split amortises the CTA's start-up over >= 512 keys
+
+__global__ void __launch_bounds__(32 * kMergeWarps)
+    ctx_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml, uint8_t* __restrict__ out,
+                     int64_t rows, int n_splits, float inv_out_scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);  // token * 32 + head
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) {
+    const float2 ml = part_ml[(int64_t)s * rows + row];
+    if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  if (mx != -INFINITY) {
+    for (int s = 0; s < n_splits; ++s) {
+      const float2 ml = part_ml[(int64_t)s * rows + row];
+      if (!(ml.y > 0.f)) continue;
+      const float w = fast_exp2(ml.x - mx);
+      const float4 o = reinterpret_cast<const float4*>(part_o + ((int64_t)s * rows + row) * kD)[lane];
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+      den = fmaf(w, ml.y, den);
+    }
+  }
+  const float inv = den > 0.f ? inv_out_scale / den : 0.f;
+  reinterpret_cast<uint32_t*>(out + row * kD)[lane] = f4_to_e4m3x4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
 std::atomic<uint64_t> g_ctx_smem_ready{0};
 
 cudaError_t ensure_ctx_smem(int dev) {
   const uint64_t bit = 1ull << (dev & 63);
   if (g_ctx_smem_ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
   cudaError_t e =
-      cudaFuncSetAttribute(ctx_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCtxSmemBytes);
+      cudaFuncSetAttribute(ctx_nvfp4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCtxSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ctx_nvfp4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCtxSmemBytes);
   if (e != cudaSuccess) return e;
   g_ctx_smem_ready.fetch_or(bit, std::memory_order_acq_rel);
   return cudaSuccess;
@@ -749,7 +838,27 @@ cudaError_t make_q_map(const uint8_t* q, int64_t total_q, CUtensorMap* map) {
 }
 }  // namespace
 
-cudaError_t launch_ctx(const CtxArgs& a, cudaStream_t stream) {
+CtxPlan plan_ctx(int64_t batch, int64_t total_q, int64_t max_pages_per_seq) {
+  CtxPlan p{0, 1};
+  if (batch < 1 || total_q < 1 || max_pages_per_seq < 1) return p;
+  // Launched units (an upper bound on the real ones, as the grid below).
+  const int64_t units = ((total_q + kQB - 1) / kQB + batch) * kHkv;
+  int64_t splits = kCtxSplitTargetCtas / units;
+  const int64_t by_len = max_pages_per_seq / kMinTilesPerSplit;
+  if (by_len < splits) splits = by_len;
+  if (splits < 2) return p;
+  const int64_t tps = (max_pages_per_seq + splits - 1) / splits;
+  p.tiles_per_split = (int)tps;
+  p.n_splits = (int)((max_pages_per_seq + tps - 1) / tps);
+  return p;
+}
+
+size_t ctx_workspace_bytes(int64_t total_q, const CtxPlan& plan) {
+  if (plan.n_splits <= 1) return 0;
+  return (size_t)plan.n_splits * (size_t)total_q * kHq * (kD * sizeof(float) + sizeof(float2));
+}
+
+cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -762,8 +871,24 @@ cudaError_t launch_ctx(const CtxArgs& a, cudaStream_t stream) {
   const int64_t grid = blocks * kHkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const float scale_log2 = a.q_scale / sqrtf((float)kD) * 1.4426950408889634f;
-  ctx_nvfp4_kernel<<<(unsigned)grid, kCtxThreads, kCtxSmemBytes, stream>>>(a, q_map, scale_log2,
-                                                                           1.f / a.out_scale);
+  const float inv_out_scale = 1.f / a.out_scale;
+  const bool split = plan.n_splits > 1;
+  if (!split) {
+    ctx_nvfp4_kernel<false><<<dim3((unsigned)grid, 1), kCtxThreads, kCtxSmemBytes, stream>>>(
+        a, q_map, scale_log2, inv_out_scale, 0, nullptr, nullptr);
+    return cudaGetLastError();
+  }
+  if (!workspace || plan.tiles_per_split < 1 || plan.n_splits > 65535) return cudaErrorInvalidValue;
+  const int64_t rows = a.total_q * kHq;
+  float* part_o = static_cast<float*>(workspace);
+  float2* part_ml = reinterpret_cast<float2*>(part_o + (size_t)plan.n_splits * rows * kD);
+  ctx_nvfp4_kernel<true><<<dim3((unsigned)grid, (unsigned)plan.n_splits), kCtxThreads, kCtxSmemBytes, stream>>>(
+      a, q_map, scale_log2, inv_out_scale, plan.tiles_per_split, part_o, part_ml);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t mblocks = (rows + kMergeWarps - 1) / kMergeWarps;
+  if (mblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  ctx_merge_kernel<<<(unsigned)mblocks, 32 * kMergeWarps, 0, stream>>>(part_o, part_ml, a.out, rows, plan.n_splits,
+                                                                      inv_out_scale);
   return cudaGetLastError();
 }
 

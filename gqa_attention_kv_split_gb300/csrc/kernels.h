@@ -62,7 +62,23 @@ struct CtxArgs {
   int64_t max_pages_per_seq;
 };
 
-cudaError_t launch_ctx(const CtxArgs& a, cudaStream_t stream);
+// Split-KV plan of the context attention, from host-known sizes only: when
+// the (sequence, 64-query block, KV head) units cannot fill the GPU (short
+// query lengths: decode-like and few-sequence calls), each unit's KV tiles
+// are divided into n_splits contiguous ranges of tiles_per_split tiles, one
+// CTA each, and a merge kernel combines the ranges' partial results.
+struct CtxPlan {
+  int tiles_per_split;  // 64-key tiles per split CTA (0 when n_splits == 1)
+  int n_splits;         // 1: the attention kernel writes the output itself
+};
+
+CtxPlan plan_ctx(int64_t batch, int64_t total_q, int64_t max_pages_per_seq);
+
+// Bytes of scratch for the split partials (0 when n_splits == 1):
+// n_splits * total_q * 32 heads * (128 f32 of O + f32 m + f32 l).
+size_t ctx_workspace_bytes(int64_t total_q, const CtxPlan& plan);
+
+cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, cudaStream_t stream);
 
 cudaError_t launch_dequant_pages(const uint8_t* fp4, const uint8_t* sf, const int32_t* block_table,
                                  const int32_t* kv_lens, uint8_t* out, int64_t batch, int64_t num_pages,

@@ -6,7 +6,7 @@ synthetic K/V (how the pages are produced), and the page scatter through a
 shuffled block table.  None of the attention or dequantisation arithmetic
 lives here: the CUDA library and the CPU oracle each do their own.
 
-The five named workloads mirror the shapes, value distributions and
+The named workloads mirror the shapes, value distributions and
 structure of the benchmark workloads this library is measured on:
 
 * decode_b2_cap256      B=2,  cap 256,    lengths {1, 200},         seed 0
@@ -14,6 +14,8 @@ structure of the benchmark workloads this library is measured on:
 * decode_b8_cap131072   B=8,  cap 131072, lengths all 131072,       seed 2, q_scale 0.5
 * ctx_b4_q2048_kv2048   batch 4, q_len = kv_len = 2048,             seed 3
 * ctx_b2_q4096_kv65536  batch 2, q_len 4096 ending a 65536-token KV, seed 4
+* ctx_b2_q1_kv4096      batch 2, q_len 1 over 4096 keys,            seed 8
+* ctx_b1_q32_kv32768    batch 1, q_len 32 over 32768 keys,          seed 9
 
 Draw order.  Decode: q, then kv, then the lengths (when random).  Context:
 Q, then K, then V, then the page permutation.  All draws come from one
@@ -219,6 +221,10 @@ DECODE_WORKLOADS = {
 CTX_WORKLOADS = {
     "ctx_b4_q2048_kv2048": dict(q_lens=[2048] * 4, kv_lens=[2048] * 4, seed=3),
     "ctx_b2_q4096_kv65536": dict(q_lens=[4096] * 2, kv_lens=[65536] * 2, seed=4),
+    # the ctx page's latency-bound GB300 rows "2 x 1 x 4096" and "1 x 32 x 32768", read as
+    # batch x q_len x kv_len: too few units to fill the GPU, so the KV range is split
+    "ctx_b2_q1_kv4096": dict(q_lens=[1, 1], kv_lens=[4096, 4096], seed=8),
+    "ctx_b1_q32_kv32768": dict(q_lens=[32], kv_lens=[32768], seed=9),
     # profiling case: one wave of 128 long units (1024 queries x 8 KV heads over 16384 keys), so that
     # counters show the steady state without per-unit start-up; not a benchmark configuration
     "ctx_b1_q1024_kv16384": dict(q_lens=[1024], kv_lens=[16384], seed=7),

@@ -165,15 +165,35 @@ gqa_status gqa_decode_plan(int64_t batch, int64_t capacity, int32_t* tokens_per_
  *   q_scale, out_scale  finite, out_scale > 0
  *
  * qo_indptr and kv_lens are read on the device only.  A query row that sees
- * no key (q_len_b > kv_len_b) is written as zeros.  P = softmax numerators
- * enter the P*V product as E4M3, so the result matches the exact value to
- * within E4M3 rounding.
+ * no key (q_len_b > kv_len_b) is written as zeros.  The softmax numerators P
+ * enter the P*V product as f16 (V's dequantised E4M3 values widened to f16
+ * exactly), so the result matches the exact value to within the output's
+ * E4M3 rounding.
+ *
+ * Work is split by (sequence, block of 64 queries, KV head).  When those
+ * units cannot fill the GPU (short query lengths: decode-like calls, few
+ * sequences), each unit's KV range is also split, as gqa_ctx_plan reports,
+ * and a second kernel merges the ranges; the partials live in the library's
+ * workspace for (device, stream) (n_splits * total_q * 32 * 520 bytes).
  */
 gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_fp4, const void* k_sf,
                                 const void* v_fp4, const void* v_sf, const int32_t* block_table,
                                 const int32_t* qo_indptr, const int32_t* kv_lens, void* out_fp8,
                                 float out_scale, int64_t batch, int64_t total_q, int64_t num_pages,
                                 int64_t max_pages_per_seq, gqa_stream_t stream);
+
+/*
+ * gqa_ctx_plan -- how nvfp4_paged_ctx_attn divides the KV range of each work
+ * unit, chosen from batch, total_q and max_pages_per_seq only (qo_indptr and
+ * kv_lens stay on the device): *tiles_per_split 64-key tiles per split CTA
+ * (0 when unsplit), *num_splits ranges per unit, *num_launches kernels per
+ * call (0 when total_q = 0; 1 unsplit; 2 with the merge).  The split is used
+ * when at most 76 units (8 KV heads x (ceil(total_q / 64) + batch)) can be
+ * launched and every range keeps at least 8 tiles.  Any output pointer may be
+ * NULL.
+ */
+gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_seq, int32_t* tiles_per_split,
+                        int32_t* num_splits, int32_t* num_launches);
 
 /*
  * gqa_debug_dequant_pages -- test export of the context kernel's NVFP4 ->

@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
     assert {"gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages", "gqa_last_error",
-            "gqa_check_device_errors", "gqa_release_workspace", "gqa_version", "gqa_decode_plan"} <= names
+            "gqa_check_device_errors", "gqa_release_workspace", "gqa_version", "gqa_decode_plan",
+            "gqa_ctx_plan"} <= names
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -116,3 +117,27 @@ def test_decode_plan_covers_capacity():
         assert p["num_launches"] == (1 if p["num_splits"] == 1 else 2)
     with pytest.raises(gqa.GqaError):
         gqa.gqa_decode_plan(0, 16)
+
+
+def test_ctx_plan_splits_only_small_calls():
+    """The context attention splits each unit's KV range only when its units
+    (8 KV heads x (ceil(total_q / 64) + batch)) leave the 152 SMs idle, into
+    at most 152 / units ranges of at least 8 tiles that cover the table."""
+    for B, tq, mp in [(2, 2, 64), (1, 32, 512), (4, 8192, 32), (2, 8192, 1024), (1, 1, 4), (1, 1, 16),
+                      (64, 64, 128), (8, 8, 2048), (1, 500, 100), (3, 5, 5), (1, 64, 16), (9, 9, 4096)]:
+        p = gqa.gqa_ctx_plan(B, tq, mp)
+        units = 8 * (-(-tq // 64) + B)
+        if p["num_splits"] == 1:
+            assert p["tiles_per_split"] == 0 and p["num_launches"] == 1
+            assert units > 76 or mp < 16
+        else:
+            assert p["num_launches"] == 2
+            assert units * p["num_splits"] <= 152
+            assert p["tiles_per_split"] >= 8
+            assert p["num_splits"] * p["tiles_per_split"] >= mp        # the ranges cover every tile
+            assert (p["num_splits"] - 1) * p["tiles_per_split"] < mp   # and none lies past the table
+    assert gqa.gqa_ctx_plan(2, 2, 64) == {"tiles_per_split": 11, "num_splits": 6, "num_launches": 2}
+    assert gqa.gqa_ctx_plan(1, 32, 512) == {"tiles_per_split": 57, "num_splits": 9, "num_launches": 2}
+    assert gqa.gqa_ctx_plan(1, 0, 16)["num_launches"] == 0
+    with pytest.raises(gqa.GqaError):
+        gqa.gqa_ctx_plan(0, 1, 16)

@@ -3,8 +3,11 @@ oracle.  Tolerance (tests/parity.py): >= 99.9 % of output elements within 2
 E4M3 ulps of E4M3(exact) and rel-L2 <= 3e-2 after dequantisation.  Cases:
 small ragged shapes spanning several 64-query units and 128-key tiles,
 decode-like rows, rows that see no key, q_scale / out_scale != 1, the
-ctx_b4_q2048_kv2048 workload in full, and ctx_b2_q4096_kv65536 on sampled
-rows in the benchmark's launch configuration."""
+split-KV path (few units: each unit's KV range divided and merged, with
+empty ranges, ragged tails and the idle second M-tile), the
+ctx_b4_q2048_kv2048, ctx_b2_q1_kv4096 and ctx_b1_q32_kv32768 workloads in
+full, and ctx_b2_q4096_kv65536 on sampled rows in the benchmark's launch
+configuration."""
 import numpy as np
 import pytest
 import torch
@@ -82,6 +85,53 @@ def test_deterministic_and_host_path():
     host = gqa.nvfp4_paged_ctx_attn(x.q_fp8, x.k_fp4, x.k_sf, x.v_fp4, x.v_sf, x.block_table, x.qo_indptr,
                                     x.kv_lens, q_scale=x.q_scale, out_scale=x.out_scale)
     assert np.array_equal(a, host.numpy())
+
+
+def plan_of(x: W.CtxInputs):
+    return gqa.gqa_ctx_plan(x.block_table.shape[0], x.q_fp8.shape[0], x.block_table.shape[1])
+
+
+# Split-KV: units too few to fill the GPU, so each unit's KV range is divided
+# and the ranges merged.  Every case asserts that the split is really taken.
+@pytest.mark.parametrize("q_lens,kv_lens", [
+    ([1], [4096]),               # decode-like: 8 ranges of 8 tiles
+    ([5, 1], [3000, 700]),       # ragged tails; the short sequence's later ranges are empty
+    ([32], [8192]),              # a single block of 32 queries: M-tile 1 is skipped
+    ([40], [2000]),              # M-tile 1 holds queries 32..39 only
+    ([33, 64], [1100, 1500]),    # several units, range boundaries inside the causal diagonal's reach
+])
+def test_split_kv_shapes(q_lens, kv_lens):
+    x = W.make_ctx_inputs(q_lens, kv_lens, seed=61 + sum(kv_lens))
+    assert plan_of(x)["num_splits"] > 1
+    check_ctx(run(x), ref(x), f"split q{q_lens} kv{kv_lens}")
+
+
+def test_split_kv_rows_without_keys_and_empty_ranges():
+    # sequence 0: 100 queries over 60 keys (queries 0..39 see none) and a single
+    # tile, so all its ranges but the first are empty; sequence 1 forces the split
+    x = W.make_ctx_inputs([100, 1], [60, 2048], seed=62)
+    assert plan_of(x)["num_splits"] > 1
+    got = run(x)
+    assert np.all(got[:40] == 0)
+    check_ctx(got, ref(x), "split, rows without keys")
+
+
+def test_split_kv_scales_and_host_path():
+    x = W.make_ctx_inputs([3], [1500], seed=63, q_scale=1.7, out_scale=0.25)
+    assert plan_of(x)["num_splits"] > 1
+    a = run(x)
+    check_ctx(a, ref(x), "split, q_scale 1.7 out_scale 0.25")
+    assert np.array_equal(a, run(x))
+    host = gqa.nvfp4_paged_ctx_attn(x.q_fp8, x.k_fp4, x.k_sf, x.v_fp4, x.v_sf, x.block_table, x.qo_indptr,
+                                    x.kv_lens, q_scale=x.q_scale, out_scale=x.out_scale)
+    assert np.array_equal(a, host.numpy())
+
+
+@pytest.mark.parametrize("name", ["ctx_b2_q1_kv4096", "ctx_b1_q32_kv32768"])
+def test_workload_split_rows_full(name):
+    x = W.ctx_workload(name)
+    assert plan_of(x)["num_splits"] > 1
+    check_ctx(run(x), ref(x), name)
 
 
 def test_workload_b4_q2048_kv2048_full():
