@@ -758,25 +758,32 @@ __global__ void __launch_bounds__(32 * kMergeWarps)
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);  // token * 32 + head
   if (row >= rows) return;
-  float mx = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) {
-    const float2 ml = part_ml[(int64_t)s * rows + row];
-    if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
-  }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  if (mx != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const float2 ml = part_ml[(int64_t)s * rows + row];
-      if (!(ml.y > 0.f)) continue;
-      const float w = fast_exp2(ml.x - mx);
-      const float4 o = reinterpret_cast<const float4*>(part_o + ((int64_t)s * rows + row) * kD)[lane];
-      acc.x = fmaf(w, o.x, acc.x);
-      acc.y = fmaf(w, o.y, acc.y);
-      acc.z = fmaf(w, o.z, acc.z);
-      acc.w = fmaf(w, o.w, acc.w);
-      den = fmaf(w, ml.y, den);
+  // lane s holds range s's (m, l) (at most 32 ranges: the plan makes <= 19)
+  float m_s = -INFINITY, l_s = 0.f;
+  if (lane < n_splits) {
+    const float2 ml = part_ml[(int64_t)lane * rows + row];
+    if (ml.y > 0.f) {
+      m_s = ml.x;
+      l_s = ml.y;
     }
+  }
+  float mx = m_s;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  const float w = l_s > 0.f ? fast_exp2(m_s - mx) : 0.f;  // mx is finite when some range saw a key
+  float den = w * l_s;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  // every range wrote its row (zeros where it saw no key), so the loads need no guard
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int s = 0; s < n_splits; ++s) {
+    const float ws = __shfl_sync(0xffffffffu, w, s);
+    const float4 o = reinterpret_cast<const float4*>(part_o + ((int64_t)s * rows + row) * kD)[lane];
+    acc.x = fmaf(ws, o.x, acc.x);
+    acc.y = fmaf(ws, o.y, acc.y);
+    acc.z = fmaf(ws, o.z, acc.z);
+    acc.w = fmaf(ws, o.w, acc.w);
   }
   const float inv = den > 0.f ? inv_out_scale / den : 0.f;
   reinterpret_cast<uint32_t*>(out + row * kD)[lane] = f4_to_e4m3x4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -838,11 +845,18 @@ cudaError_t make_q_map(const uint8_t* q, int64_t total_q, CUtensorMap* map) {
 }
 }  // namespace
 
+// Upper bound on the number of (sequence, 64-query block) units without
+// reading qo_indptr on the host: sum_b ceil(q_b / 64) = sum_b floor((q_b + 63)
+// / 64) <= floor((total_q + 63 batch) / 64).
+static int64_t max_query_blocks(int64_t batch, int64_t total_q) {
+  return (total_q + (int64_t)(kQB - 1) * batch) / kQB;
+}
+
 CtxPlan plan_ctx(int64_t batch, int64_t total_q, int64_t max_pages_per_seq) {
   CtxPlan p{0, 1};
   if (batch < 1 || total_q < 1 || max_pages_per_seq < 1) return p;
   // Launched units (an upper bound on the real ones, as the grid below).
-  const int64_t units = ((total_q + kQB - 1) / kQB + batch) * kHkv;
+  const int64_t units = max_query_blocks(batch, total_q) * kHkv;
   int64_t splits = kCtxSplitTargetCtas / units;
   const int64_t by_len = max_pages_per_seq / kMinTilesPerSplit;
   if (by_len < splits) splits = by_len;
@@ -865,10 +879,7 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
   if ((e = ensure_ctx_smem(dev)) != cudaSuccess) return e;
   alignas(64) CUtensorMap q_map;
   if ((e = make_q_map(a.q, a.total_q, &q_map)) != cudaSuccess) return e;
-  // Upper bound on the number of (sequence, 64-query block) units without
-  // reading qo_indptr on the host: sum_b ceil(q_len_b / 64) <= total_q / 64 + batch.
-  const int64_t blocks = (a.total_q + kQB - 1) / kQB + a.batch;
-  const int64_t grid = blocks * kHkv;
+  const int64_t grid = max_query_blocks(a.batch, a.total_q) * kHkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const float scale_log2 = a.q_scale / sqrtf((float)kD) * 1.4426950408889634f;
   const float inv_out_scale = 1.f / a.out_scale;
@@ -878,7 +889,8 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
         a, q_map, scale_log2, inv_out_scale, 0, nullptr, nullptr);
     return cudaGetLastError();
   }
-  if (!workspace || plan.tiles_per_split < 1 || plan.n_splits > 65535) return cudaErrorInvalidValue;
+  // the merge holds one range per lane
+  if (!workspace || plan.tiles_per_split < 1 || plan.n_splits > 32) return cudaErrorInvalidValue;
   const int64_t rows = a.total_q * kHq;
   float* part_o = static_cast<float*>(workspace);
   float2* part_ml = reinterpret_cast<float2*>(part_o + (size_t)plan.n_splits * rows * kD);

@@ -188,8 +188,9 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
  * kv_lens stay on the device): *tiles_per_split 64-key tiles per split CTA
  * (0 when unsplit), *num_splits ranges per unit, *num_launches kernels per
  * call (0 when total_q = 0; 1 unsplit; 2 with the merge).  The split is used
- * when at most 76 units (8 KV heads x (ceil(total_q / 64) + batch)) can be
- * launched and every range keeps at least 8 tiles.  Any output pointer may be
+ * when at most 76 units (8 KV heads x floor((total_q + 63 * batch) / 64), a
+ * bound on the (sequence, 64-query block) pairs) can be launched and every
+ * range keeps at least 8 tiles.  Any output pointer may be
  * NULL.
  */
 gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_seq, int32_t* tiles_per_split,

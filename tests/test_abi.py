@@ -121,12 +121,13 @@ def test_decode_plan_covers_capacity():
 
 def test_ctx_plan_splits_only_small_calls():
     """The context attention splits each unit's KV range only when its units
-    (8 KV heads x (ceil(total_q / 64) + batch)) leave the 152 SMs idle, into
-    at most 152 / units ranges of at least 8 tiles that cover the table."""
+    (8 KV heads x floor((total_q + 63 batch) / 64), a bound on the sequences'
+    64-query blocks) leave the 152 SMs idle, into at most 152 / units ranges
+    of at least 8 tiles that cover the table."""
     for B, tq, mp in [(2, 2, 64), (1, 32, 512), (4, 8192, 32), (2, 8192, 1024), (1, 1, 4), (1, 1, 16),
                       (64, 64, 128), (8, 8, 2048), (1, 500, 100), (3, 5, 5), (1, 64, 16), (9, 9, 4096)]:
         p = gqa.gqa_ctx_plan(B, tq, mp)
-        units = 8 * (-(-tq // 64) + B)
+        units = 8 * ((tq + 63 * B) // 64)
         if p["num_splits"] == 1:
             assert p["tiles_per_split"] == 0 and p["num_launches"] == 1
             assert units > 76 or mp < 16
@@ -136,8 +137,8 @@ def test_ctx_plan_splits_only_small_calls():
             assert p["tiles_per_split"] >= 8
             assert p["num_splits"] * p["tiles_per_split"] >= mp        # the ranges cover every tile
             assert (p["num_splits"] - 1) * p["tiles_per_split"] < mp   # and none lies past the table
-    assert gqa.gqa_ctx_plan(2, 2, 64) == {"tiles_per_split": 11, "num_splits": 6, "num_launches": 2}
-    assert gqa.gqa_ctx_plan(1, 32, 512) == {"tiles_per_split": 57, "num_splits": 9, "num_launches": 2}
+    assert gqa.gqa_ctx_plan(2, 2, 64) == {"tiles_per_split": 8, "num_splits": 8, "num_launches": 2}
+    assert gqa.gqa_ctx_plan(1, 32, 512) == {"tiles_per_split": 27, "num_splits": 19, "num_launches": 2}
     assert gqa.gqa_ctx_plan(1, 0, 16)["num_launches"] == 0
     with pytest.raises(gqa.GqaError):
         gqa.gqa_ctx_plan(0, 1, 16)
