@@ -735,6 +735,9 @@ __global__ void __launch_bounds__(kCtxThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc::fence_before_thread_sync();
   __syncthreads();
+  // Split-KV: the partials are written; let the merge grid be launched (it
+  // waits for this grid's completion before it reads them).
+  if constexpr (kSplit) asm volatile("griddepcontrol.launch_dependents;");
   if (warp == 1) {
     tc::fence_after_thread_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -757,6 +760,9 @@ __global__ void __launch_bounds__(32 * kMergeWarps)
                      int64_t rows, int n_splits, float inv_out_scale) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);  // token * 32 + head
+  // Launched as a programmatic dependent of the attention kernel: wait until
+  // that grid has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (row >= rows) return;
   // lane s holds range s's (m, l) (at most 32 ranges: the plan makes <= 19)
   float m_s = -INFINITY, l_s = 0.f;
@@ -899,9 +905,20 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t mblocks = (rows + kMergeWarps - 1) / kMergeWarps;
   if (mblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  ctx_merge_kernel<<<(unsigned)mblocks, 32 * kMergeWarps, 0, stream>>>(part_o, part_ml, a.out, rows, plan.n_splits,
-                                                                      inv_out_scale);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge's launch overlaps the attention
+  // kernel's tail (the merge waits for it with griddepcontrol.wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)mblocks);
+  cfg.blockDim = dim3(32 * kMergeWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ctx_merge_kernel, (const float*)part_o, (const float2*)part_ml, a.out, rows,
+                            plan.n_splits, inv_out_scale);
 }
 
 cudaError_t ctx_read_errors(uint32_t* word) {
