@@ -332,6 +332,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   } else {
     reinterpret_cast<float4*>(part_o + (row * n_splits + s) * kD)[lane] = acc;
     if (lane == 0) part_ml[row * n_splits + s] = make_float2(M, L);
+    // the partials are written: the merge grid may be launched (it waits for
+    // this grid's completion before it reads them)
+    asm volatile("griddepcontrol.launch_dependents;");
   }
 }
 
@@ -355,6 +358,9 @@ __global__ void __launch_bounds__(128)
     if (warp == 0) reinterpret_cast<uint2*>(out + row * kD)[lane] = make_uint2(0u, 0u);
     return;
   }
+  // Launched as a programmatic dependent of the split kernel: wait until that
+  // grid has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float2* ml = part_ml + row * n_splits;
   float M = -INFINITY;
   for (int s = warp; s < nv; s += 4) M = fmaxf(M, ml[s].x);
@@ -462,10 +468,22 @@ cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens
       static_cast<__half*>(out), capacity, plan.chunk, plan.n_splits, scale_log2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (plan.n_splits > 1) {
-    dim3 mgrid(kHq, (unsigned)batch);
-    decode_merge_kernel<<<mgrid, 128, 0, stream>>>(part_o, part_ml, seq_lens, static_cast<__half*>(out),
-                                                   capacity, plan.chunk, plan.n_splits);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // programmatic dependent launch: the merge's launch and its seq_lens read
+    // overlap the split kernel's last CTAs (griddepcontrol.wait orders the rest)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kHq, (unsigned)batch);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, (const float*)part_o, (const float2*)part_ml, seq_lens,
+                                static_cast<__half*>(out), (int64_t)capacity, (int)plan.chunk,
+                                (int)plan.n_splits)) != cudaSuccess)
+      return e;
   }
   return cudaSuccess;
 }
