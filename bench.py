@@ -216,7 +216,15 @@ def run_gpu(args):
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
     dx = W.decode_workload(dec_name, device=dev) if run_decode else None
+    paged = isinstance(dx, W.PagedDecodeInputs)
     dec_out = torch.empty_like(dx.q) if dx is not None else None
+
+    def decode_call(q, kv_like, lens, out):
+        # kv_like: the stacked kv tensor, or (k_pages, v_pages, block_table) of a paged cache
+        if paged:
+            gqa.gqa_decode_paged(q, *kv_like, lens, out=out, q_scale=dx.q_scale)
+        else:
+            gqa.gqa_decode(q, kv_like, lens, out=out, q_scale=dx.q_scale)
     cx = W.ctx_workload(ctx_name, device=dev) if run_ctx else None
     ctx_args = None
     ctx_out = None
@@ -235,7 +243,7 @@ def run_gpu(args):
     def step(evs):
         if dx is not None:
             evs[0].record(stream)
-            gqa.gqa_decode(dx.q, dx.kv, dx.seq_lens, out=dec_out, q_scale=dx.q_scale)
+            decode_call(dx.q, (dx.k_pages, dx.v_pages, dx.block_table) if paged else dx.kv, dx.seq_lens, dec_out)
             evs[1].record(stream)
         if ctx_ok:
             flush.zero_()
@@ -270,26 +278,34 @@ def run_gpu(args):
     # of the output inside the timed region, every step.
     e2e = None
     if rank == 0 and dx is not None:
-        hq, hkv, hl = dx.q.cpu().pin_memory(), dx.kv.cpu().pin_memory(), dx.seq_lens.cpu().pin_memory()
+        hq, hl = dx.q.cpu().pin_memory(), dx.seq_lens.cpu().pin_memory()
+        if paged:
+            hkv = tuple(t.cpu().pin_memory() for t in (dx.k_pages, dx.v_pages, dx.block_table))
+        else:
+            hkv = dx.kv.cpu().pin_memory()
         hout = torch.empty_like(hq).pin_memory()
         for _ in range(2):
-            gqa.gqa_decode(hq, hkv, hl, out=hout, q_scale=dx.q_scale)
+            decode_call(hq, hkv, hl, hout)
         n_e2e = max(3, min(args.steps, 10))
         ts = []
         for _ in range(n_e2e):
             a, b = _events(torch, 2)
             a.record(stream)
-            gqa.gqa_decode(hq, hkv, hl, out=hout, q_scale=dx.q_scale)
+            decode_call(hq, hkv, hl, hout)
             b.record(stream)
             torch.cuda.synchronize()
             ts.append(a.elapsed_time(b))
         lens = hl.clamp(0, dx.capacity).to(torch.int64)
-        h2d = hq.numel() * 2 + int(lens.sum()) * 16 * 256 + hl.numel() * 4
+        if paged:  # the host path stages every page and the table
+            h2d = hq.numel() * 2 + sum(t.numel() * t.element_size() for t in hkv) + hl.numel() * 4
+        else:      # the host path stages each sequence's first len tokens
+            h2d = hq.numel() * 2 + int(lens.sum()) * 16 * 256 + hl.numel() * 4
         d2h = hout.numel() * 2
         e2e_ms = statistics.fmean(ts)
         e2e = {"value": round(dx.kv_bytes_read() / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-               "steps": n_e2e, "path": "gqa_decode with pinned host buffers"}
+               "steps": n_e2e,
+               "path": ("gqa_decode_paged" if paged else "gqa_decode") + " with pinned host buffers"}
         del hkv
 
     if rank != 0:
@@ -302,12 +318,15 @@ def run_gpu(args):
     n_launch_ctx = ctx_plan["num_launches"] if (ctx_plan is not None and ctx_ok) else 0
     if dx is not None:
         gbs = dx.kv_bytes_read() * world / (dec_max * 1e-3) / 1e9
-        traffic = profiled_traffic("decode_split_kernel_decode_b64_cap8192.md", ["decode.cu", "common.cuh"])
+        # the committed counters were taken on decode_b64_cap8192 only
+        traffic = (profiled_traffic("decode_split_kernel_decode_b64_cap8192.md", ["decode.cu", "common.cuh"])
+                   if dec_name == DECODE_WL else None)
         line.update({
             "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dec_max + ctx_max, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic",
             "config": {"workload": dec_name, "batch": dx.batch, "capacity": dx.capacity, "q_heads": 32,
+                       "kv_layout": "64-token HND pages, shuffled block table" if paged else "stacked [B,2,8,cap,128]",
                        "kv_heads": 8, "head_dim": 128, "kv_bytes_read_per_step": dx.kv_bytes_read(),
                        "l2": "decode inputs larger than L2; L2 flushed (512 MB write) before each ctx call",
                        "parallelism": f"replicas{world}",
@@ -364,7 +383,19 @@ def run_gpu(args):
 def _decode_sample(dx, n_seq):
     import gqa_workloads as W
     idx = list(range(n_seq))
+    if isinstance(dx, W.PagedDecodeInputs):  # the pages stay whole; the table rows are sampled
+        return W.PagedDecodeInputs(dx.q[idx].cpu(), dx.k_pages.cpu(), dx.v_pages.cpu(), dx.block_table[idx].cpu(),
+                                   dx.seq_lens[idx].cpu(), dx.q_scale)
     return W.DecodeInputs(dx.q[idx].cpu(), dx.kv[idx].cpu(), dx.seq_lens[idx].cpu(), dx.q_scale)
+
+
+def _oracle_decode(sub, threads):
+    import gqa_workloads as W
+    import oracle
+    if isinstance(sub, W.PagedDecodeInputs):
+        return oracle.gqa_decode_paged(sub.q.numpy(), sub.k_pages.numpy(), sub.v_pages.numpy(),
+                                       sub.block_table.numpy(), sub.seq_lens.numpy(), sub.q_scale, threads=threads)
+    return oracle.gqa_decode(sub.q.numpy(), sub.kv.numpy(), sub.seq_lens.numpy(), sub.q_scale, threads=threads)
 
 
 def oracle_decode_sample(dx, budget_s=15.0):
@@ -376,7 +407,7 @@ def oracle_decode_sample(dx, budget_s=15.0):
     while True:
         sub = _decode_sample(dx, n)
         t0 = time.perf_counter()
-        oracle.gqa_decode(sub.q.numpy(), sub.kv.numpy(), sub.seq_lens.numpy(), sub.q_scale, threads=threads)
+        _oracle_decode(sub, threads)
         took = time.perf_counter() - t0
         if n >= dx.batch or took >= budget_s / 3:
             break
@@ -440,7 +471,11 @@ def run_reference(args):
         cfg = {"workload": name}
     else:
         dx = W.decode_workload(name, device="cuda" if torch.cuda.is_available() else "cpu")
-        dx = W.DecodeInputs(dx.q.cpu(), dx.kv.cpu(), dx.seq_lens.cpu(), dx.q_scale)
+        if isinstance(dx, W.PagedDecodeInputs):
+            dx = W.PagedDecodeInputs(*(t.cpu() for t in (dx.q, dx.k_pages, dx.v_pages, dx.block_table, dx.seq_lens)),
+                                     dx.q_scale)
+        else:
+            dx = W.DecodeInputs(dx.q.cpu(), dx.kv.cpu(), dx.seq_lens.cpu(), dx.q_scale)
         per_step = max(1, args.ref_seqs or 2)
         import oracle
         threads = oracle.default_threads()
@@ -448,9 +483,13 @@ def run_reference(args):
         for i in range(args.warmup + args.steps):
             lo = (i * per_step) % dx.batch
             idx = [(lo + k) % dx.batch for k in range(per_step)]
-            sub = W.DecodeInputs(dx.q[idx], dx.kv[idx], dx.seq_lens[idx], dx.q_scale)
+            if isinstance(dx, W.PagedDecodeInputs):
+                sub = W.PagedDecodeInputs(dx.q[idx].cpu(), dx.k_pages.cpu(), dx.v_pages.cpu(),
+                                          dx.block_table[idx].cpu(), dx.seq_lens[idx].cpu(), dx.q_scale)
+            else:
+                sub = W.DecodeInputs(dx.q[idx].cpu(), dx.kv[idx].cpu(), dx.seq_lens[idx].cpu(), dx.q_scale)
             t0 = time.perf_counter()
-            oracle.gqa_decode(sub.q.numpy(), sub.kv.numpy(), sub.seq_lens.numpy(), sub.q_scale, threads=threads)
+            _oracle_decode(sub, threads)
             dt = time.perf_counter() - t0
             if i >= args.warmup:
                 times.append(dt)

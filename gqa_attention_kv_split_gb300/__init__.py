@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "GqaError", "lib", "gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages",
-    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_noalloc", "LIB_PATH",
+    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_paged", "gqa_decode_noalloc", "LIB_PATH",
     "build",
 ]
 
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.gqa_ctx_plan.argtypes = [i64, i64, i64, c.POINTER(c.c_int32), c.POINTER(c.c_int32),
                                        c.POINTER(c.c_int32)]
             L.gqa_ctx_plan.restype = c.c_int
+            L.gqa_decode_paged.argtypes = [vp, vp, vp, i32p, i32p, vp, i64, i64, i64, f32, vp]
+            L.gqa_decode_paged.restype = c.c_int
             L.gqa_release_workspace.argtypes = []
             L.gqa_release_workspace.restype = c.c_int
             _lib = L
@@ -134,6 +136,31 @@ def gqa_decode(q: torch.Tensor, kv: torch.Tensor, seq_lens: torch.Tensor, *, out
         out = torch.empty_like(q)
     _need(out, "out", (torch.float16,), (B, HQ, D))
     _check(lib().gqa_decode(_p(q), _p(kv), _p(seq_lens), _p(out), B, kv.shape[3], float(q_scale), _stream_for(q)))
+    return out
+
+
+def gqa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                     seq_lens: torch.Tensor, *, out: torch.Tensor | None = None, q_scale: float = 1.0) -> torch.Tensor:
+    """gqa_decode over a paged K/V cache (see include/gqa.h): q [B,32,128]
+    f16, k_pages / v_pages [num_pages,8,64,128] f16, block_table
+    [B, max_pages_per_seq] int32, seq_lens [B] int32, all on one CUDA device
+    or all on the host."""
+    B = q.shape[0]
+    _need(q, "q", (torch.float16,), (B, HQ, D))
+    if k_pages.dim() != 4:
+        raise ValueError("k_pages must be [num_pages, 8, 64, 128]")
+    P = k_pages.shape[0]
+    _need(k_pages, "k_pages", (torch.float16,), (P, HKV, 64, D))
+    _need(v_pages, "v_pages", (torch.float16,), (P, HKV, 64, D))
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [batch, max_pages_per_seq]")
+    _need(block_table, "block_table", (torch.int32,), (B, block_table.shape[1]))
+    _need(seq_lens, "sequence_lengths", (torch.int32,), (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.float16,), (B, HQ, D))
+    _check(lib().gqa_decode_paged(_p(q), _p(k_pages), _p(v_pages), _p(block_table), _p(seq_lens), _p(out), B, P,
+                                  block_table.shape[1], float(q_scale), _stream_for(q)))
     return out
 
 

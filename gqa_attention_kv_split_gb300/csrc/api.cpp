@@ -238,6 +238,86 @@ gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, vo
   return GQA_OK;
 }
 
+gqa_status gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                            const int32_t* seq_lens, void* out, int64_t batch, int64_t num_pages,
+                            int64_t max_pages_per_seq, float q_scale, gqa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (batch < 1 || batch > 65535) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 65535]", (long long)batch);
+  if (num_pages < 1 || num_pages > 2147483647LL)
+    return fail(GQA_ERR_INVALID_ARG, "num_pages %lld out of range", (long long)num_pages);
+  if (max_pages_per_seq < 1 || max_pages_per_seq > (2147483647LL / 64))
+    return fail(GQA_ERR_INVALID_ARG, "max_pages_per_seq %lld out of range", (long long)max_pages_per_seq);
+  if (!std::isfinite(q_scale)) return fail(GQA_ERR_INVALID_ARG, "q_scale is not finite");
+  Where where;
+  gqa_status st = locate({{q, "q", 16},
+                          {k_pages, "k_pages", 16},
+                          {v_pages, "v_pages", 16},
+                          {block_table, "block_table", 4},
+                          {seq_lens, "seq_lens", 4},
+                          {out, "out", 16}},
+                         &where);
+  if (st != GQA_OK) return st;
+  const int64_t capacity = max_pages_per_seq * 64;
+  const gqa::DecodePlan plan = gqa::plan_decode(batch, capacity);
+  if (plan.n_splits < 1) return fail(GQA_ERR_INVALID_ARG, "launch grid must be positive");
+  const size_t part_bytes = gqa::decode_workspace_bytes(batch, plan);
+  gqa::DecodePages pg;
+  pg.num_pages = num_pages;
+  pg.max_pages_per_seq = max_pages_per_seq;
+
+  if (!where.host) {
+    ScopedDevice sd(where.device);
+    if (!sd.ok()) return fail(GQA_ERR_CUDA, "cannot switch to device %d", where.device);
+    void* ws = nullptr;
+    if ((st = workspace(where.device, stream, part_bytes, &ws)) != GQA_OK) return st;
+    pg.k_pages = k_pages;
+    pg.v_pages = v_pages;
+    pg.block_table = block_table;
+    GQA_CUDA_TRY(gqa::launch_decode_paged(q, pg, seq_lens, out, batch, q_scale, plan, ws, stream),
+                 "paged decode launch");
+    return GQA_OK;
+  }
+
+  // Host buffers: the host can read the lengths and the table, so check the
+  // pages a sequence uses, then stage everything and run.
+  for (int64_t b = 0; b < batch; ++b) {
+    int64_t len = seq_lens[b];
+    len = len < 0 ? 0 : (len > capacity ? capacity : len);
+    for (int64_t p = 0; p < (len + 63) / 64; ++p) {
+      const int32_t pgid = block_table[b * max_pages_per_seq + p];
+      if (pgid < 0 || pgid >= num_pages)
+        return fail(GQA_ERR_INVALID_ARG, "block_table[%lld][%lld] = %d outside [0, num_pages)", (long long)b,
+                    (long long)p, pgid);
+    }
+  }
+  int dev = 0;
+  GQA_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  const size_t q_bytes = (size_t)batch * 32 * 128 * 2;
+  const size_t page_bytes = (size_t)num_pages * 8 * 64 * 128 * 2;
+  const size_t bt_bytes = (size_t)batch * max_pages_per_seq * 4;
+  Carver c;
+  const size_t o_q = c.take(q_bytes), o_k = c.take(page_bytes), o_v = c.take(page_bytes), o_bt = c.take(bt_bytes),
+               o_len = c.take((size_t)batch * 4), o_out = c.take(q_bytes), o_part = c.take(part_bytes);
+  void* ws = nullptr;
+  if ((st = workspace(dev, stream, c.off, &ws)) != GQA_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const std::pair<size_t, std::pair<const void*, size_t>> copies[] = {
+      {o_q, {q, q_bytes}},       {o_k, {k_pages, page_bytes}},        {o_v, {v_pages, page_bytes}},
+      {o_bt, {block_table, bt_bytes}}, {o_len, {seq_lens, (size_t)batch * 4}}};
+  for (const auto& cp : copies)
+    GQA_CUDA_TRY(cudaMemcpyAsync(base + cp.first, cp.second.first, cp.second.second, cudaMemcpyHostToDevice, stream),
+                 "stage input");
+  pg.k_pages = base + o_k;
+  pg.v_pages = base + o_v;
+  pg.block_table = reinterpret_cast<const int32_t*>(base + o_bt);
+  GQA_CUDA_TRY(gqa::launch_decode_paged(base + o_q, pg, reinterpret_cast<const int32_t*>(base + o_len), base + o_out,
+                                        batch, q_scale, plan, part_bytes ? base + o_part : nullptr, stream),
+               "paged decode launch");
+  GQA_CUDA_TRY(cudaMemcpyAsync(out, base + o_out, q_bytes, cudaMemcpyDeviceToHost, stream), "copy out");
+  GQA_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+  return GQA_OK;
+}
+
 gqa_status gqa_decode_noalloc(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
                               int64_t capacity, float q_scale, gqa_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

@@ -71,8 +71,11 @@ __device__ __forceinline__ void h8_to_f8(const uint4& u, float f[8]) {
   }
 }
 
+// kPaged: K/V come from 64-token HND pages through a block table (pages;
+// kv unused); otherwise from the stacked cache kv [B, 2, 8, cap, 128].
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 3)
-    decode_split_kernel(const __half* __restrict__ q, const __half* __restrict__ kv,
+    decode_split_kernel(const __half* __restrict__ q, const __half* __restrict__ kv, const DecodePages pages,
                         const int32_t* __restrict__ seq_lens, float* __restrict__ part_o,
                         float2* __restrict__ part_ml, __half* __restrict__ out, int64_t cap, int chunk,
                         int n_splits, float scale_log2) {
@@ -110,6 +113,46 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   __syncthreads();
 
+  if (warp == kComputeWarps && kPaged) {
+    // ---------------- producer (paged): a 16-token stage lies inside one
+    // 64-token page (t0 is a multiple of 64).  The whole warp reads the
+    // chunk's page numbers 32 at a time, one group ahead; lane 0 issues the
+    // copies of each stage from (page, g, token % 64).
+    const uint64_t pol = policy_evict_first();
+    const int32_t* bt = pages.block_table + (int64_t)b * pages.max_pages_per_seq + t0 / kPage;
+    const int n_pg = (n_tok + kPage - 1) / kPage;
+    int cur = lane < n_pg ? bt[lane] : 0;
+    int nxt = 32 + lane < n_pg ? bt[32 + lane] : 0;
+    const __half* kp = static_cast<const __half*>(pages.k_pages);
+    const __half* vp = static_cast<const __half*>(pages.v_pages);
+    for (int i = 0; i < n_st; ++i) {
+      const int pi = i / (kPage / kStageTok);  // page of this stage within the chunk
+      if (pi > 0 && (pi & 31) == 0 && i % (kPage / kStageTok) == 0) {
+        cur = nxt;
+        nxt = pi + 32 + lane < n_pg ? bt[pi + 32 + lane] : 0;
+      }
+      int page = __shfl_sync(0xffffffffu, cur, pi & 31);
+      const int st = i % kStages;
+      if (i >= kStages &&
+          !__all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1, &g_decode_err)))
+        break;
+      if (lane == 0) {
+        if (page < 0 || page >= pages.num_pages) {
+          atomicOr(&g_decode_err, kErrBadIndex);
+          page = 0;
+        }
+        const int nt = min(kStageTok, n_tok - i * kStageTok);
+        const uint32_t bytes = (uint32_t)nt * kRowBytes;
+        const int64_t off = (((int64_t)page * kHkv + g) * kPage + (i % (kPage / kStageTok)) * kStageTok) * kD;
+        const uint32_t fb = smem_u32(&sm.full[st]);
+        mbar_arrive_expect_tx(fb, 2 * bytes);
+        bulk_g2s_hint(smem_u32(sm.k[st]), kp + off, bytes, fb, pol);
+        bulk_g2s_hint(smem_u32(sm.v[st]), vp + off, bytes, fb, pol);
+      }
+      __syncwarp();
+    }
+    return;
+  }
   if (warp == kComputeWarps) {
     // ---------------- producer: bulk copies of K and V tiles --------------
     if (lane == 0) {
@@ -409,8 +452,11 @@ std::atomic<uint64_t> g_smem_ready{0};  // per-device bit: smem opt-in done
 cudaError_t ensure_smem_optin(int dev) {
   const uint64_t bit = 1ull << (dev & 63);
   if (g_smem_ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sizeof(DecodeSmem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sizeof(DecodeSmem));
   if (e != cudaSuccess) return e;
   g_smem_ready.fetch_or(bit, std::memory_order_acq_rel);
   return cudaSuccess;
@@ -447,9 +493,10 @@ size_t decode_workspace_bytes(int64_t batch, const DecodePlan& plan) {
   return rows * kD * sizeof(float) + rows * sizeof(float2);
 }
 
-cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
-                          int64_t capacity, float q_scale, const DecodePlan& plan, void* workspace,
-                          cudaStream_t stream) {
+namespace {
+cudaError_t launch_decode_any(const void* q, const void* kv, const DecodePages* pages, const int32_t* seq_lens,
+                              void* out, int64_t batch, int64_t capacity, float q_scale, const DecodePlan& plan,
+                              void* workspace, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -463,9 +510,15 @@ cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens
     part_ml = reinterpret_cast<float2*>(part_o + rows * kD);
   }
   dim3 grid((unsigned)plan.n_splits, kHkv, (unsigned)batch);
-  decode_split_kernel<<<grid, kThreads, sizeof(DecodeSmem), stream>>>(
-      static_cast<const __half*>(q), static_cast<const __half*>(kv), seq_lens, part_o, part_ml,
-      static_cast<__half*>(out), capacity, plan.chunk, plan.n_splits, scale_log2);
+  if (pages) {
+    decode_split_kernel<true><<<grid, kThreads, sizeof(DecodeSmem), stream>>>(
+        static_cast<const __half*>(q), nullptr, *pages, seq_lens, part_o, part_ml, static_cast<__half*>(out),
+        capacity, plan.chunk, plan.n_splits, scale_log2);
+  } else {
+    decode_split_kernel<false><<<grid, kThreads, sizeof(DecodeSmem), stream>>>(
+        static_cast<const __half*>(q), static_cast<const __half*>(kv), DecodePages{}, seq_lens, part_o, part_ml,
+        static_cast<__half*>(out), capacity, plan.chunk, plan.n_splits, scale_log2);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (plan.n_splits > 1) {
     // programmatic dependent launch: the merge's launch and its seq_lens read
@@ -486,6 +539,20 @@ cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens
       return e;
   }
   return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
+                          int64_t capacity, float q_scale, const DecodePlan& plan, void* workspace,
+                          cudaStream_t stream) {
+  return launch_decode_any(q, kv, nullptr, seq_lens, out, batch, capacity, q_scale, plan, workspace, stream);
+}
+
+cudaError_t launch_decode_paged(const void* q, const DecodePages& pages, const int32_t* seq_lens, void* out,
+                                int64_t batch, float q_scale, const DecodePlan& plan, void* workspace,
+                                cudaStream_t stream) {
+  return launch_decode_any(q, nullptr, &pages, seq_lens, out, batch, pages.max_pages_per_seq * kPage, q_scale,
+                           plan, workspace, stream);
 }
 
 // ---- allocation-free variant ---------------------------------------------

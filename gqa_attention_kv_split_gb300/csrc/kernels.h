@@ -22,6 +22,23 @@ DecodePlan plan_decode(int64_t batch, int64_t capacity);
 // (0 when a single split covers the capacity).
 size_t decode_workspace_bytes(int64_t batch, const DecodePlan& plan);
 
+// Paged K/V for the decode: 64-token pages in HND order, one block table row
+// per sequence (the same page layout as the context attention's NVFP4
+// pages, with fp16 values).
+struct DecodePages {
+  const void* k_pages;         // [num_pages, 8, 64, 128] f16
+  const void* v_pages;         // [num_pages, 8, 64, 128] f16
+  const int32_t* block_table;  // [batch, max_pages_per_seq]
+  int64_t num_pages;
+  int64_t max_pages_per_seq;   // capacity = 64 * max_pages_per_seq
+};
+
+// The paged decode: the same split-KV kernels, K/V tiles gathered through
+// the block table (capacity = 64 * pages.max_pages_per_seq).
+cudaError_t launch_decode_paged(const void* q, const DecodePages& pages, const int32_t* seq_lens, void* out,
+                                int64_t batch, float q_scale, const DecodePlan& plan, void* workspace,
+                                cudaStream_t stream);
+
 cudaError_t launch_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
                           int64_t capacity, float q_scale, const DecodePlan& plan, void* workspace,
                           cudaStream_t stream);

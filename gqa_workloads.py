@@ -12,6 +12,8 @@ structure of the benchmark workloads this library is measured on:
 * decode_b2_cap256      B=2,  cap 256,    lengths {1, 200},         seed 0
 * decode_b64_cap8192    B=64, cap 8192,   lengths U{1..8192},       seed 1
 * decode_b8_cap131072   B=8,  cap 131072, lengths all 131072,       seed 2, q_scale 0.5
+* decode_paged_<name>   any of the above re-laid out into 64-token HND pages through a
+                        shuffled block table (randperm seeded with seed + 1000)
 * ctx_b4_q2048_kv2048   batch 4, q_len = kv_len = 2048,             seed 3
 * ctx_b2_q4096_kv65536  batch 2, q_len 4096 ending a 65536-token KV, seed 4
 * ctx_b2_q1_kv4096      batch 2, q_len 1 over 4096 keys,            seed 8
@@ -69,6 +71,53 @@ def make_decode_inputs(batch: int, capacity: int, seq_lens=None, *, seed: int, q
     else:
         lens = torch.tensor(list(seq_lens), dtype=torch.int32, device=device)
     return DecodeInputs(q, kv, lens, float(q_scale))
+
+
+@dataclass
+class PagedDecodeInputs:
+    """The stacked workload re-laid out into 64-token HND pages."""
+    q: torch.Tensor            # [B, 32, 128] float16
+    k_pages: torch.Tensor      # [num_pages, 8, 64, 128] float16
+    v_pages: torch.Tensor
+    block_table: torch.Tensor  # [B, capacity / 64] int32
+    seq_lens: torch.Tensor     # [B] int32
+    q_scale: float
+
+    @property
+    def batch(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def capacity(self) -> int:
+        return self.block_table.shape[1] * PAGE
+
+    def kv_bytes_read(self) -> int:
+        """K/V bytes the kernels read: 4096 per token (8 heads x 128 x 2 B x K,V)."""
+        n = self.seq_lens.clamp(0, self.capacity).to(torch.int64).sum().item()
+        return int(n) * HKV * D * 2 * 2
+
+
+def page_decode_inputs(x: DecodeInputs, *, seed: int, shuffle: bool = True) -> PagedDecodeInputs:
+    """Scatter a stacked decode workload into 64-token pages, physical page of
+    (b, logical page p) = perm[b * (cap / 64) + p] (a randperm drawn after the
+    stacked workload's draws, or the identity)."""
+    B, cap = x.batch, x.capacity
+    assert cap % PAGE == 0
+    mp = cap // PAGE
+    dev = x.q.device
+    if shuffle:
+        g = torch.Generator(device=dev).manual_seed(seed + 1000)
+        perm = torch.randperm(B * mp, generator=g, device=dev)
+    else:
+        perm = torch.arange(B * mp, device=dev)
+    k_pages = torch.empty(B * mp, HKV, PAGE, D, dtype=torch.float16, device=dev)
+    v_pages = torch.empty_like(k_pages)
+    for b in range(B):  # [8, cap, 128] -> [mp, 8, 64, 128]
+        phys = perm[b * mp:(b + 1) * mp]
+        k_pages[phys] = x.kv[b, 0].view(HKV, mp, PAGE, D).permute(1, 0, 2, 3)
+        v_pages[phys] = x.kv[b, 1].view(HKV, mp, PAGE, D).permute(1, 0, 2, 3)
+    block_table = perm.view(B, mp).to(torch.int32)
+    return PagedDecodeInputs(x.q, k_pages, v_pages, block_table, x.seq_lens, x.q_scale)
 
 
 # -------------------------------------------------------------- NVFP4 ctx ---
@@ -231,7 +280,13 @@ CTX_WORKLOADS = {
 }
 
 
-def decode_workload(name: str, device="cpu") -> DecodeInputs:
+def decode_workload(name: str, device="cpu"):
+    """A stacked decode workload, or (decode_paged_*) the same draws re-laid
+    out into pages through a shuffled block table."""
+    if name.startswith("decode_paged_"):
+        base = "decode_" + name[len("decode_paged_"):]
+        spec = DECODE_WORKLOADS[base]
+        return page_decode_inputs(make_decode_inputs(**spec, device=device), seed=spec["seed"])
     return make_decode_inputs(**DECODE_WORKLOADS[name], device=device)
 
 

@@ -122,6 +122,37 @@ gqa_status gqa_decode_noalloc(const void* q, const void* kv, const int32_t* seq_
                               int64_t capacity, float q_scale, gqa_stream_t stream);
 
 /*
+ * gqa_decode_paged -- the operation of gqa_decode over a paged K/V cache:
+ * the same split-KV kernels, each 16-token K/V tile gathered through the
+ * block table ("NVIDIA SM110 GPU를 위한 실험적인 FP16 GQA 디코드 커널 추가",
+ * section 1, for the operation; the page layout is the one the context
+ * attention uses, "GB300 NVFP4 Context Attention: scale slot 조기 반납과 8단
+ * packed K/V ring", introduction, with fp16 values).
+ *
+ *   q            [batch, 32, 128]                 fp16
+ *   k_pages      [num_pages, 8, 64, 128]          fp16, HND: page p, KV head g,
+ *   v_pages      [num_pages, 8, 64, 128]          slot s holds token 64*p' + s
+ *                of the sequence whose block_table row maps logical page p'
+ *                to p
+ *   block_table  [batch, max_pages_per_seq]       int32; entries for logical
+ *                pages < ceil(len_b / 64) must be in [0, num_pages)
+ *   seq_lens     [batch]                          int32, read on the device,
+ *                clamped to [0, 64 * max_pages_per_seq]
+ *   out          [batch, 32, 128]                 fp16, written
+ *
+ * Splits as gqa_decode_plan(batch, 64 * max_pages_per_seq) reports.  Same
+ * placement rules as gqa_decode (one device, or all host buffers: staged,
+ * synchronous, table entries checked on the host).  A page index outside
+ * [0, num_pages) met on the device is not read: page 0 is used instead and
+ * bit 1 of the error word (gqa_check_device_errors) is set.  Errors:
+ * GQA_ERR_UNSUPPORTED for batch outside [1, 65535], GQA_ERR_INVALID_ARG for
+ * bad sizes, NULL or misaligned pointers, a non-finite q_scale.
+ */
+gqa_status gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                            const int32_t* seq_lens, void* out, int64_t batch, int64_t num_pages,
+                            int64_t max_pages_per_seq, float q_scale, gqa_stream_t stream);
+
+/*
  * gqa_decode_plan -- how gqa_decode splits the KV sequence for a given batch
  * and capacity (chosen from these two only; the lengths stay on the device):
  * *tokens_per_split tokens per split CTA, *num_splits splits per sequence,

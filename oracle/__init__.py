@@ -160,6 +160,37 @@ def gqa_decode(q_f16, kv_f16, seq_lens, q_scale: float = 1.0, items=None, thread
     return out
 
 
+def gqa_decode_paged(q_f16, k_pages, v_pages, block_table, seq_lens, q_scale: float = 1.0, items=None,
+                     threads: int | None = None):
+    """fp64 decode attention over a paged K/V cache: the decode of the SM110
+    FP16 GQA decode page (section 1) with K/V held in 64-token HND pages
+    ("GB300 NVFP4 Context Attention ...", introduction, for the layout).
+    Token t of sequence b is slot t % 64 of page block_table[b, t // 64],
+    KV head g of that page; the sequence's tokens are gathered into the
+    stacked [B, 2, 8, cap, 128] cache (cap = 64 * table width) and go through
+    gqa_decode above.
+
+    k_pages, v_pages: [num_pages, 8, 64, 128] float16 (or uint16 bits);
+    block_table: [B, max_pages] int32; seq_lens: [B] int32.
+    """
+    kp = np.asarray(k_pages)
+    vp = np.asarray(v_pages)
+    kp = kp.view(np.uint16) if kp.dtype == np.float16 else kp
+    vp = vp.view(np.uint16) if vp.dtype == np.float16 else vp
+    bt = np.asarray(block_table).astype(np.int64)
+    sl = np.asarray(seq_lens).astype(np.int32)
+    B, mp = bt.shape
+    cap = mp * 64
+    kv = np.zeros((B, 2, HKV, cap, D), dtype=np.uint16)
+    for b in range(B):
+        n = min(max(int(sl[b]), 0), cap)
+        for p in range((n + 63) // 64):
+            pg = bt[b, p]
+            kv[b, 0, :, 64 * p:64 * p + 64, :] = kp[pg]  # [8, 64, 128]: head, slot, d
+            kv[b, 1, :, 64 * p:64 * p + 64, :] = vp[pg]
+    return gqa_decode(q_f16, kv, sl, q_scale, items=items, threads=threads)
+
+
 # ------------------------------------------------------------------- ctx ---
 
 def dequant_pages(fp4_pages, sf_pages, block_table, kv_lens, max_kv: int | None = None) -> np.ndarray:

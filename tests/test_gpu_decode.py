@@ -3,7 +3,9 @@
 Tolerance: max |err| <= 1e-2 and rel-L2 <= 2e-3 (tests/parity.py).  Cases
 span one and many splits, ragged tails, empty and clamped lengths, the
 shapes of the decode page's benchmark tables, and the full-size workloads
-in the launch configuration the benchmark times (sampled rows)."""
+in the launch configuration the benchmark times (sampled rows); and the
+paged decode (gqa_decode_paged): against the oracle, bit-identical to the
+stacked decode of the same draws, host buffers, a flagged bad page index."""
 import numpy as np
 import pytest
 import torch
@@ -122,3 +124,68 @@ def test_workload_b8_cap131072_sampled():
     x = W.decode_workload("decode_b8_cap131072", device=DEV)
     assert x.kv.numel() == 2 ** 31  # 64-bit offsets exercised
     _sampled_check(x, [0, 7], "decode_b8_cap131072")
+
+
+# ---- paged decode ---------------------------------------------------------
+
+def run_paged(p: W.PagedDecodeInputs, dev=DEV):
+    out = gqa.gqa_decode_paged(*[t.to(dev) for t in (p.q, p.k_pages, p.v_pages, p.block_table, p.seq_lens)],
+                               q_scale=p.q_scale)
+    if dev is not None and dev.type == "cuda":
+        torch.cuda.synchronize()
+    return out.cpu()
+
+
+def ref_paged(p: W.PagedDecodeInputs):
+    return oracle.gqa_decode_paged(p.q.numpy(), p.k_pages.numpy(), p.v_pages.numpy(), p.block_table.numpy(),
+                                   p.seq_lens.numpy(), p.q_scale)
+
+
+@pytest.mark.parametrize("batch,cap,lens,seed", [
+    (3, 256, [1, 200, 256], 81),                                    # one split
+    (4, 4096, [4096, 1, 2999, 0], 82),                              # split + merge, empty sequence
+    (6, 1000 // 64 * 64 + 64, [0, 1, 64, 65, 1000, 1024], 83),      # ragged page tails
+])
+def test_paged_matches_oracle(batch, cap, lens, seed):
+    p = W.page_decode_inputs(W.make_decode_inputs(batch, cap, lens, seed=seed), seed=seed)
+    check_decode(run_paged(p).double().numpy(), ref_paged(p), f"paged B{batch} cap{cap}")
+
+
+def test_paged_is_bit_identical_to_stacked():
+    """The paged kernel reads the same 16-token tiles in the same order as the
+    stacked one, so the two agree bit for bit on a re-laid-out workload."""
+    x = W.make_decode_inputs(5, 2048, [2048, 1, 700, 1999, 64], seed=84)
+    p = W.page_decode_inputs(x, seed=84)
+    assert torch.equal(run(x), run_paged(p))
+
+
+def test_paged_host_buffers_match_device_path():
+    p = W.page_decode_inputs(W.make_decode_inputs(2, 512, [500, 33], seed=85), seed=85)
+    host = gqa.gqa_decode_paged(p.q, p.k_pages, p.v_pages, p.block_table, p.seq_lens, q_scale=p.q_scale)
+    assert torch.equal(host, run_paged(p))
+
+
+def test_paged_bad_page_index_is_flagged_not_read():
+    """A table entry outside [0, num_pages) met on the device: page 0 is read
+    instead and bit 1 of the error word is set (no out-of-bounds access)."""
+    p = W.page_decode_inputs(W.make_decode_inputs(1, 128, [100], seed=86), seed=86)
+    bt = p.block_table.clone()
+    bt[0, 1] = 1 << 20
+    gqa.gqa_decode_paged(p.q.to(DEV), p.k_pages.to(DEV), p.v_pages.to(DEV), bt.to(DEV), p.seq_lens.to(DEV),
+                         q_scale=p.q_scale)
+    assert gqa.gqa_check_device_errors(0) & 2
+
+
+def test_workload_paged_b64_cap8192_bit_identical_and_sampled():
+    """The benchmark's paged workload: bit-identical to the stacked decode of
+    the same draws, and sampled rows against the oracle."""
+    x = W.decode_workload("decode_b64_cap8192", device="cuda")
+    p = W.decode_workload("decode_paged_b64_cap8192", device="cuda")
+    a = gqa.gqa_decode(x.q, x.kv, x.seq_lens, q_scale=x.q_scale)
+    b = gqa.gqa_decode_paged(p.q, p.k_pages, p.v_pages, p.block_table, p.seq_lens, q_scale=p.q_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    seqs = [0, 17, 63]
+    sub = W.PagedDecodeInputs(p.q[seqs].cpu(), p.k_pages.cpu(), p.v_pages.cpu(), p.block_table[seqs].cpu(),
+                              p.seq_lens[seqs].cpu(), p.q_scale)
+    check_decode(b[seqs].cpu().double().numpy(), ref_paged(sub), "decode_paged_b64_cap8192 sampled")

@@ -95,3 +95,50 @@ def test_token_permutation_invariance():
     a = oracle.gqa_decode(x.q.numpy(), x.kv.numpy(), x.seq_lens.numpy())
     b = oracle.gqa_decode(x.q.numpy(), kv2.numpy(), x.seq_lens.numpy())
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+# ---- paged decode: the gather through the block table -------------------
+
+def test_paged_identity_table_equals_stacked():
+    """With pages laid out in order (block table = 0, 1, 2, ...), the paged
+    oracle sees exactly the stacked cache: bit-identical fp64 results."""
+    x = W.make_decode_inputs(3, 256, [1, 200, 256], seed=71)
+    p = W.page_decode_inputs(x, seed=71, shuffle=False)
+    assert np.array_equal(p.block_table.numpy().ravel(), np.arange(12))
+    d = oracle.gqa_decode(x.q.numpy(), x.kv.numpy(), x.seq_lens.numpy(), x.q_scale)
+    g = oracle.gqa_decode_paged(p.q.numpy(), p.k_pages.numpy(), p.v_pages.numpy(), p.block_table.numpy(),
+                                p.seq_lens.numpy(), p.q_scale)
+    assert np.array_equal(d, g)
+
+
+def test_paged_result_is_independent_of_page_placement():
+    """Shuffling the physical pages (and the table with them) changes nothing."""
+    x = W.make_decode_inputs(2, 320, [320, 77], seed=72)
+    a = W.page_decode_inputs(x, seed=72, shuffle=False)
+    b = W.page_decode_inputs(x, seed=72, shuffle=True)
+    assert not np.array_equal(a.block_table.numpy(), b.block_table.numpy())
+    ra = oracle.gqa_decode_paged(a.q.numpy(), a.k_pages.numpy(), a.v_pages.numpy(), a.block_table.numpy(),
+                                 a.seq_lens.numpy(), a.q_scale)
+    rb = oracle.gqa_decode_paged(b.q.numpy(), b.k_pages.numpy(), b.v_pages.numpy(), b.block_table.numpy(),
+                                 b.seq_lens.numpy(), b.q_scale)
+    assert np.array_equal(ra, rb)
+
+
+def test_paged_ignores_slots_past_the_length_and_unused_pages():
+    """Slots of the last page past the length, pages the table does not reach
+    and table entries past the last page do not enter the result; a page used
+    by a token does (the gather reads the right slot)."""
+    x = W.make_decode_inputs(2, 256, [70, 130], seed=73)
+    p = W.page_decode_inputs(x, seed=73)
+    ref = oracle.gqa_decode_paged(p.q.numpy(), p.k_pages.numpy(), p.v_pages.numpy(), p.block_table.numpy(),
+                                  p.seq_lens.numpy(), p.q_scale)
+    kp, vp, bt = p.k_pages.numpy().copy(), p.v_pages.numpy().copy(), p.block_table.numpy().copy()
+    kp[bt[0, 1], :, 6:] = np.float16(300.0)   # sequence 0 holds 70 tokens: page 1, slots 6.. unused
+    vp[bt[0, 1], :, 6:] = np.float16(-300.0)
+    kp[bt[0, 2]] = np.float16(123.0)          # page 2 of sequence 0 is never reached
+    bt[1, 3] = 10 ** 6                        # entry past sequence 1's last page (130 tokens: pages 0..2)
+    got = oracle.gqa_decode_paged(p.q.numpy(), kp, vp, bt, p.seq_lens.numpy(), p.q_scale)
+    assert np.array_equal(ref, got)
+    vp[bt[0, 1], :, 5] = np.float16(50.0)     # token 69 = page 1, slot 5: it is read
+    moved = oracle.gqa_decode_paged(p.q.numpy(), kp, vp, bt, p.seq_lens.numpy(), p.q_scale)
+    assert not np.allclose(moved[0], ref[0]) and np.array_equal(moved[1], ref[1])
