@@ -44,6 +44,12 @@
 //    from the exact result; an f16 P costs no more tensor time than the
 //    two E4M3 terms (hi + lo) it would take to match it, and one conversion
 //    per two weights instead of a split.
+//  * Split-KV (ctx_nvfp4_kernel<true>): when the units cannot fill the GPU
+//    (short query lengths, few sequences), grid.y divides each unit's KV
+//    tiles into contiguous ranges; each range writes its unnormalised O and
+//    (m, l) in f32, and ctx_merge_kernel, launched as a programmatic
+//    dependent grid, combines them by their maxima.  A unit whose queries
+//    all lie in M-tile 0 leaves M-tile 1 idle in both instances.
 #include <cuda.h>  // CUtensorMap and the cuTensorMapEncodeTiled prototype (resolved at run time)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
