@@ -32,7 +32,7 @@ def test_header_declares_the_entry_points():
     names = set(declared_functions())
     assert {"gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages", "gqa_last_error",
             "gqa_check_device_errors", "gqa_release_workspace", "gqa_version", "gqa_decode_plan",
-            "gqa_ctx_plan"} <= names
+            "gqa_ctx_plan", "gqa_decode_paged"} <= names
 
 
 def test_library_exports_every_declared_symbol(L):
@@ -78,6 +78,24 @@ def test_ctx_rejects_bad_sizes_and_nulls(L):
     null_kv = [f, 1.0, f, f, f, f, f, f, P(0), f, 1.0]
     assert L.nvfp4_paged_ctx_attn(*null_kv, 1, 16, 4, 2, s) == INVALID
     assert b"kv_lens" in L.gqa_last_error()
+
+
+def test_paged_decode_rejects_bad_sizes_and_nulls(L):
+    s = P(0)
+    f = fake()
+    # q, k_pages, v_pages, block_table, seq_lens, out, batch, num_pages, max_pages_per_seq, q_scale
+    assert L.gqa_decode_paged(f, f, f, f, f, f, 0, 4, 2, 1.0, s) == UNSUPPORTED
+    assert b"batch" in L.gqa_last_error()
+    assert L.gqa_decode_paged(f, f, f, f, f, f, 70000, 4, 2, 1.0, s) == UNSUPPORTED
+    assert L.gqa_decode_paged(f, f, f, f, f, f, 1, 0, 2, 1.0, s) == INVALID
+    assert b"num_pages" in L.gqa_last_error()
+    assert L.gqa_decode_paged(f, f, f, f, f, f, 1, 4, 0, 1.0, s) == INVALID
+    assert L.gqa_decode_paged(f, f, f, f, f, f, 1, 4, 1 << 26, 1.0, s) == INVALID  # capacity past 2^31 - 1
+    assert L.gqa_decode_paged(f, f, f, f, f, f, 1, 4, 2, float("nan"), s) == INVALID
+    assert L.gqa_decode_paged(f, P(0), f, f, f, f, 1, 4, 2, 1.0, s) == INVALID
+    assert b"k_pages is a null pointer" in L.gqa_last_error()
+    assert L.gqa_decode_paged(f, f, f, P(0), f, f, 1, 4, 2, 1.0, s) == INVALID
+    assert b"block_table" in L.gqa_last_error()
 
 
 def test_dequant_rejects_bad_sizes(L):

@@ -189,3 +189,14 @@ def test_workload_paged_b64_cap8192_bit_identical_and_sampled():
     sub = W.PagedDecodeInputs(p.q[seqs].cpu(), p.k_pages.cpu(), p.v_pages.cpu(), p.block_table[seqs].cpu(),
                               p.seq_lens[seqs].cpu(), p.q_scale)
     check_decode(b[seqs].cpu().double().numpy(), ref_paged(sub), "decode_paged_b64_cap8192 sampled")
+
+
+def test_paged_decode_host_path_checks_the_table():
+    """With host buffers the library reads the lengths and the table: a used
+    entry outside [0, num_pages) is rejected before anything is staged."""
+    import torch
+    q = torch.zeros(1, 32, 128, dtype=torch.float16)
+    pages = torch.zeros(2, 8, 64, 128, dtype=torch.float16)
+    bt = torch.tensor([[0, 5]], dtype=torch.int32)       # page 5 does not exist
+    with pytest.raises(gqa.GqaError, match="block_table"):
+        gqa.gqa_decode_paged(q, pages, pages, bt, torch.tensor([100], dtype=torch.int32))
