@@ -12,15 +12,15 @@
  *  - "NVIDIA SM110 GPU를 위한 실험적인 FP16 GQA 디코드 커널 추가" (FlashInfer
  *    PR #5052 analysis), section 1 (the sm110_gqa_decode API docstring:
  *    q [batch,32,128], kv [batch,2,8,capacity,128], int32 sequence_lengths,
- *    q_scale applied before the standard 1/sqrt(128)), section 2 (fixed
- *    32/8/128 configuration) and section 3 (the SDPA comparator with
- *    enable_gqa=True, scale 1/sqrt(128)).
+ *    the caller's q_scale in front of the usual 1/sqrt(128) factor),
+ *    section 2 (fixed 32/8/128 configuration) and section 3 (the SDPA
+ *    comparator with enable_gqa=True, scale 1/sqrt(128)).
  *  - "GB300 NVFP4 Context Attention: scale slot 조기 반납과 8단 packed K/V
  *    ring" (FlashInfer PR #9177 analysis), introduction: FP8-E4M3 query and
  *    output, NVFP4 K/V pages with E4M3 block scales dequantised to E4M3,
  *    head dim 128, bottom-right causal mask, HND page layout.
  *
- * Readings taken where the pages are silent (each is restated in the design doc):
+ * Readings taken where the pages are silent:
  *  - GQA head mapping: query head h reads KV head h / 4 (contiguous groups,
  *    the enable_gqa convention of the SDPA comparator).
  *  - A decode length of 0 yields a zero row; lengths are clamped to
@@ -28,7 +28,7 @@
  *  - E2M1 nibble order: element 2i sits in the low nibble of byte i.
  *  - Block scale layout: sf[page, kv_head, slot, d / 16], same HND order as
  *    the data.
- *  - "Dequantise to E4M3": the exact product e2m1(code) * e4m3(scale) is
+ *  - Dequantisation target: the exact product e2m1(code) * e4m3(scale) is
  *    rounded to E4M3, round-to-nearest-even, saturating at +-448.
  *  - Context attention scale: q_scale / sqrt(128), as for decode.  The output
  *    is O / out_scale (the caller dequantises with out = out_fp8 * out_scale).
