@@ -152,15 +152,23 @@ __device__ void find_unit(const int32_t* __restrict__ qo, int B, int t, int& out
   const int lane = threadIdx.x & 31;
   out_b = -1;
   out_qb = -1;
+  int nqb0 = 0;  // blocks of sequence lane, read once (the rounds below reuse it)
+  if (lane < B) {
+    const int ql = qo[lane + 1] - qo[lane];
+    nqb0 = ql > 0 ? (ql + kQB - 1) / kQB : 0;
+  }
   for (int r = 0;; ++r) {
     int cnt = 0;
     bool any = false;
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int b = b0 + lane;
-      int nqb = 0;
-      if (b < B) {
-        const int ql = qo[b + 1] - qo[b];
-        nqb = ql > 0 ? (ql + kQB - 1) / kQB : 0;
+      int nqb = nqb0;
+      if (b0 > 0) {
+        nqb = 0;
+        if (b < B) {
+          const int ql = qo[b + 1] - qo[b];
+          nqb = ql > 0 ? (ql + kQB - 1) / kQB : 0;
+        }
       }
       const unsigned bal = __ballot_sync(0xffffffffu, nqb > r);
       const int c = __popc(bal);
