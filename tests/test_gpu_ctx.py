@@ -87,6 +87,16 @@ def test_deterministic_and_host_path():
     assert np.array_equal(a, host.numpy())
 
 
+def test_many_sequences_and_empty_queries():
+    """40 sequences (the unit lookup walks two groups of 32), some with no
+    query rows, ragged query and KV lengths."""
+    rng = np.random.default_rng(64)
+    q_lens = [int(v) for v in rng.choice([0, 1, 7, 33, 64, 70], size=40)]
+    kv_lens = [q + int(k) for q, k in zip(q_lens, rng.integers(0, 150, size=40))]
+    x = W.make_ctx_inputs(q_lens, kv_lens, seed=64)
+    check_ctx(run(x), ref(x), "40 sequences")
+
+
 def plan_of(x: W.CtxInputs):
     return gqa.gqa_ctx_plan(x.block_table.shape[0], x.q_fp8.shape[0], x.block_table.shape[1])
 
