@@ -177,7 +177,7 @@ extern "C" {
 
 const char* gqa_last_error(void) { return t_last_error.c_str(); }
 
-int gqa_version(void) { return 100; }
+int gqa_version(void) { return 200; }  // 0.2.0: gqa_decode_paged, gqa_ctx_plan, split-KV context attention
 
 gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
                       int64_t capacity, float q_scale, gqa_stream_t stream_) {
