@@ -126,6 +126,26 @@ def test_python_binding_checks_shapes_and_dtypes():
                        torch.zeros(1, 2, 4, 4, 128, dtype=torch.float16), torch.ones(1, dtype=torch.int32))
 
 
+def test_python_binding_checks_paged_decode_arguments():
+    import torch
+    q = torch.zeros(1, 32, 128, dtype=torch.float16)
+    pages = torch.zeros(3, 8, 64, 128, dtype=torch.float16)
+    bt = torch.zeros(1, 2, dtype=torch.int32)
+    lens = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(TypeError):   # pages must be fp16
+        gqa.gqa_decode_paged(q, pages.float(), pages, bt, lens)
+    with pytest.raises(ValueError):  # 64-token pages of 8 heads
+        gqa.gqa_decode_paged(q, torch.zeros(3, 8, 32, 128, dtype=torch.float16), pages, bt, lens)
+    with pytest.raises(ValueError):  # K and V pages alike
+        gqa.gqa_decode_paged(q, pages, torch.zeros(2, 8, 64, 128, dtype=torch.float16), bt, lens)
+    with pytest.raises(ValueError):  # one table row per sequence
+        gqa.gqa_decode_paged(q, pages, pages, torch.zeros(2, 2, dtype=torch.int32), lens)
+    with pytest.raises(TypeError):   # int32 table
+        gqa.gqa_decode_paged(q, pages, pages, bt.long(), lens)
+    with pytest.raises(ValueError):  # contiguous
+        gqa.gqa_decode_paged(q, pages, pages, torch.zeros(1, 4, dtype=torch.int32)[:, ::2], lens)
+
+
 def test_decode_plan_covers_capacity():
     for B, cap in [(2, 256), (64, 8192), (8, 131072), (1, 1), (3, 1000)]:
         p = gqa.gqa_decode_plan(B, cap)
