@@ -507,6 +507,56 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def measure_peaks(seconds_sustained: float = 4.0) -> dict:
+    """Context figures for the rooflines, on this GPU: a read-only HBM stream
+    (sum of a 4 GiB tensor), dense GEMMs 8192^3 in bf16 (torch.matmul) and in
+    FP8 E4M3 with bf16 output (torch._scaled_mm): best of 10, and the FP8 GEMM
+    again in a loop of `seconds_sustained` seconds.  The rooflines bench.py
+    reports keep the measured copy bandwidth and bf16 x 2 as their peaks."""
+    import torch
+    dev = torch.device("cuda:0")
+    out = {}
+
+    def best_ms(fn, reps=10):
+        ts = []
+        for _ in range(reps + 2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(); fn(); b.record(); torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return min(ts[2:])
+
+    x = torch.ones(2 * 1024 ** 3, dtype=torch.bfloat16, device=dev)  # 4 GiB
+    ms = best_ms(lambda: x.sum())
+    out["hbm_read_gbs"] = round(x.numel() * 2 / (ms * 1e-3) / 1e9, 1)
+    del x
+    n = 8192
+    a = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    ms = best_ms(lambda: torch.matmul(a, b))
+    out["bf16_tflops"] = round(2 * n ** 3 / (ms * 1e-3) / 1e12, 1)
+    try:
+        a8 = a.to(torch.float8_e4m3fn)
+        b8 = b.to(torch.float8_e4m3fn).t().contiguous().t()  # column-major second operand
+        one = torch.ones((), device=dev, dtype=torch.float32)
+        f8 = lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        ms = best_ms(f8)
+        out["fp8_tflops"] = round(2 * n ** 3 / (ms * 1e-3) / 1e12, 1)
+        cnt, t0 = 0, time.perf_counter()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        while time.perf_counter() - t0 < seconds_sustained:
+            for _ in range(50):
+                f8()
+            cnt += 50
+            torch.cuda.synchronize()
+        s1.record(); torch.cuda.synchronize()
+        out["fp8_tflops_sustained"] = round(2 * n ** 3 * cnt / (s0.elapsed_time(s1) * 1e-3) / 1e12, 1)
+    except Exception as e:  # noqa: BLE001 -- report why, keep the other figures
+        out["fp8_error"] = f"{type(e).__name__}: {e}"[:200]
+    out["device"] = torch.cuda.get_device_name(dev)
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -518,7 +568,18 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-seqs", type=int, default=0, help="reference arm: sequences per step (decode)")
     ap.add_argument("--ref-rows", type=int, default=0, help="reference arm: (row, head) items per step (ctx)")
+    ap.add_argument("--peaks", action="store_true",
+                    help="measure context peaks (read-only HBM stream, bf16 and FP8 GEMMs) and exit")
     args = ap.parse_args(argv)
+    if args.peaks:
+        with ClockSampler(0) as clk:
+            time.sleep(0.3)
+            clk.mark("start")
+            res = measure_peaks()
+            clk.mark("stop")
+        res["clocks"] = clk.summary()
+        print(json.dumps(res))
+        return
     if args.warmup < 3 and args.impl == "ours":
         print("note: warm-up raised to the minimum of 3 steps", file=sys.stderr)
         args.warmup = 3
