@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "GqaError", "lib", "gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages",
-    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_paged", "gqa_decode_noalloc", "LIB_PATH",
+    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_paged", "gqa_debug_wait_expiry", "gqa_decode_noalloc", "LIB_PATH",
     "build",
 ]
 
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
             L.gqa_ctx_plan.restype = c.c_int
             L.gqa_decode_paged.argtypes = [vp, vp, vp, i32p, i32p, vp, i64, i64, i64, f32, vp]
             L.gqa_decode_paged.restype = c.c_int
+            L.gqa_debug_wait_expiry.argtypes = [c.c_int, vp]
+            L.gqa_debug_wait_expiry.restype = c.c_int
             L.gqa_release_workspace.argtypes = []
             L.gqa_release_workspace.restype = c.c_int
             _lib = L
@@ -236,6 +238,14 @@ def gqa_ctx_plan(batch: int, total_q: int, max_pages_per_seq: int) -> dict:
     _check(lib().gqa_ctx_plan(int(batch), int(total_q), int(max_pages_per_seq), ctypes.byref(t), ctypes.byref(n),
                               ctypes.byref(l)))
     return {"tiles_per_split": t.value, "num_splits": n.value, "num_launches": l.value}
+
+
+def gqa_debug_wait_expiry(device: int = 0) -> None:
+    """Launch the failure-detection check (see include/gqa.h): one wait that
+    nothing completes expires after about 2 s and sets bit 0 of the error word."""
+    import torch
+    stream = torch.cuda.current_stream(device).cuda_stream
+    _check(lib().gqa_debug_wait_expiry(int(device), ctypes.c_void_p(stream)))
 
 
 def gqa_check_device_errors(device: int = 0) -> int:

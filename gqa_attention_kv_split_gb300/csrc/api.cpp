@@ -503,6 +503,13 @@ gqa_status gqa_debug_dequant_pages(const void* fp4, const void* sf, const int32_
   return GQA_OK;
 }
 
+gqa_status gqa_debug_wait_expiry(int device, gqa_stream_t stream) {
+  ScopedDevice sd(device);
+  if (!sd.ok()) return fail(GQA_ERR_CUDA, "cannot switch to device %d", device);
+  GQA_CUDA_TRY(gqa::launch_wait_expiry(reinterpret_cast<cudaStream_t>(stream)), "wait-expiry launch");
+  return GQA_OK;
+}
+
 gqa_status gqa_check_device_errors(int device, uint32_t* word) {
   if (!word) return fail(GQA_ERR_INVALID_ARG, "word is a null pointer");
   *word = 0;

@@ -555,6 +555,28 @@ cudaError_t launch_decode_paged(const void* q, const DecodePages& pages, const i
                            plan, workspace, stream);
 }
 
+// ---- bounded-wait check ---------------------------------------------------
+//
+// One thread waits on an mbarrier that nothing completes, through the same
+// bounded wait every kernel here uses: after kWaitNs it records
+// kErrWaitTimeout in the error word and returns.  No trap, no fault; the
+// context stays usable.
+namespace {
+__global__ void wait_expiry_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    mbar_wait(smem_u32(&bar), 0, &g_decode_err);  // phase 0 never completes
+  }
+}
+}  // namespace
+
+cudaError_t launch_wait_expiry(cudaStream_t stream) {
+  wait_expiry_kernel<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
+}
+
 // ---- allocation-free variant ---------------------------------------------
 //
 // Scratch for gqa_decode_noalloc: the per-split partials live in this

@@ -55,6 +55,10 @@ cudaError_t launch_decode_static_scratch(const void* q, const void* kv, const in
                                          int64_t batch, int64_t capacity, float q_scale, const DecodePlan& plan,
                                          cudaStream_t stream);
 
+// Test export: one CTA whose single wait never completes; its bounded wait
+// expires after kWaitNs and sets kErrWaitTimeout in the decode error word.
+cudaError_t launch_wait_expiry(cudaStream_t stream);
+
 // Reads and clears the decode kernels' device error word on the current
 // device (synchronises the device).
 cudaError_t decode_read_errors(uint32_t* word);

@@ -251,6 +251,16 @@ gqa_status gqa_debug_dequant_pages(const void* fp4, const void* sf, const int32_
  */
 gqa_status gqa_check_device_errors(int device, uint32_t* word);
 
+/*
+ * gqa_debug_wait_expiry -- test export of the kernels' failure detection: on
+ * `device`, one CTA waits on an mbarrier that nothing completes, through the
+ * bounded wait every kernel of the library uses.  After about 2 s the wait
+ * gives up, sets bit 0 of the error word and the kernel returns; a following
+ * gqa_check_device_errors reports GQA_ERR_TIMEOUT.  No trap and no fault: the
+ * context stays usable.  Asynchronous on `stream`.
+ */
+gqa_status gqa_debug_wait_expiry(int device, gqa_stream_t stream);
+
 /* Free every workspace the library holds (all devices and streams).  The
  * caller must ensure no libgqa work is still running. */
 gqa_status gqa_release_workspace(void);

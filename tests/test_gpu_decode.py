@@ -200,3 +200,19 @@ def test_paged_decode_host_path_checks_the_table():
     bt = torch.tensor([[0, 5]], dtype=torch.int32)       # page 5 does not exist
     with pytest.raises(gqa.GqaError, match="block_table"):
         gqa.gqa_decode_paged(q, pages, pages, bt, torch.tensor([100], dtype=torch.int32))
+
+
+def test_bounded_wait_expires_and_is_reported():
+    """Failure detection without a fault: a wait that nothing completes gives
+    up after ~2 s, the host reads GQA_ERR_TIMEOUT (bit 0), and the context is
+    still usable afterwards."""
+    import time
+    assert gqa.gqa_check_device_errors(0) == 0
+    t0 = time.perf_counter()
+    gqa.gqa_debug_wait_expiry(0)
+    word = gqa.gqa_check_device_errors(0)   # synchronises; returns and clears the word
+    took = time.perf_counter() - t0
+    assert word & 1 and 1.5 < took < 30
+    assert gqa.gqa_check_device_errors(0) == 0
+    x = W.decode_workload("decode_b2_cap256")
+    check_decode(run(x).double().numpy(), ref(x), "decode after an expired wait")
