@@ -24,6 +24,7 @@
 //    (m, l, o[128]) per (b, h, split); a second tiny kernel merges the splits
 //    by log-sum-exp.  When one split covers the capacity, the split kernel
 //    normalises and writes fp16 directly and no merge is launched.
+#include <cuda.h>  // CUcontext and the cuCtxGetCurrent prototype (resolved at run time)
 #include <cuda_fp16.h>
 
 #include <atomic>
@@ -474,11 +475,6 @@ DecodePlan plan_decode(int64_t batch, int64_t capacity) {
   const double per_split = (double)batch * kHkv * (double)capacity / 4096.0;
   int chunk = 256;
   while (chunk < 4096 && chunk < per_split) chunk *= 2;
-  if (const char* env = getenv("GQA_DECODE_SPLIT_TOKENS")) {
-    int v = atoi(env);
-    if (v >= kChunkQuantum) chunk = v;
-  }
-  chunk = (chunk + kChunkQuantum - 1) / kChunkQuantum * kChunkQuantum;
   const int64_t cap_q = (capacity + kChunkQuantum - 1) / kChunkQuantum * kChunkQuantum;
   if (cap_q <= chunk) chunk = (int)(cap_q > 0 ? cap_q : kChunkQuantum);
   p.chunk = chunk;
@@ -583,13 +579,39 @@ cudaError_t launch_wait_expiry(cudaStream_t stream) {
 // file-scope device array instead of a cudaMalloc'd workspace.  Every GPU
 // that loads the library holds it until the process exits.  In host code the
 // name g_static_scratch is only a stand-in for the symbol, never a device
-// address: the address is looked up once per device (with that device
-// current) by cudaGetSymbolAddress and cached.
+// address: the address is looked up by cudaGetSymbolAddress (with the device
+// current) and cached per device together with the CUDA context it belongs
+// to.  A device reset destroys the primary context and reloads the module
+// at a possibly different address, so a call that finds another context
+// current looks the address up again.
 static __device__ __align__(256) uint8_t g_static_scratch[kDecodeStaticScratchBytes];
 
 namespace {
 std::mutex g_static_mu;
-void* g_static_addr[64] = {};
+struct StaticScratchAddr {
+  void* addr = nullptr;
+  CUcontext ctx = nullptr;
+};
+StaticScratchAddr g_static_addr[64];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+std::once_flag g_ctx_fn_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+
+// The calling thread's current CUDA context (nullptr if the driver entry
+// point is unavailable: the cache is then keyed by device alone).
+CUcontext current_context() {
+  std::call_once(g_ctx_fn_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+  });
+  CUcontext c = nullptr;
+  if (g_ctx_get_current && g_ctx_get_current(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
 }  // namespace
 
 cudaError_t launch_decode_static_scratch(const void* q, const void* kv, const int32_t* seq_lens, void* out,
@@ -603,13 +625,16 @@ cudaError_t launch_decode_static_scratch(const void* q, const void* kv, const in
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_static_mu);
-    if (g_static_addr[dev] == nullptr) {
+    const CUcontext ctx = current_context();
+    StaticScratchAddr& c = g_static_addr[dev];
+    if (c.addr == nullptr || c.ctx != ctx) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_static_scratch);
       if (e != cudaSuccess) return e;
-      g_static_addr[dev] = p;
+      c.addr = p;
+      c.ctx = current_context();  // the lookup may have created the primary context
     }
-    scratch = g_static_addr[dev];
+    scratch = c.addr;
   }
   // The partials need no clearing: the merge reads only the splits that the
   // split kernel of this same call has written.

@@ -110,8 +110,11 @@ gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, vo
  *     520 bytes, splits as reported by gqa_decode_plan.  The benchmark shapes
  *     (64 x 8192, 8 x 131072) need 8.5 MB.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) and caches it; make that first call before any
- *     stream capture.
+ *     (cudaGetSymbolAddress) and caches it with the device's current CUDA
+ *     context; a call that finds another context current (after
+ *     cudaDeviceReset, which reloads the library's device code) looks it up
+ *     again.  Make the first call on a device, and the first after a reset,
+ *     before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind (nothing in it needs to start at zero).  Calls whose kernels
  *     overlap on the GPU -- on different streams, without ordering -- race on

@@ -5,11 +5,15 @@ Tolerances (stated by the benchmark specification of this library):
   fp64 oracle.
 * FP8 context output: >= 99.9 % of elements within 2 E4M3 ulps of the
   oracle's exact value rounded to E4M3, and relative L2 error <= 3e-2 after
-  dequantisation.  The ulp distance is the difference of the monotone code
-  ordinals.  Where the E4M3 output format itself cannot meet 3e-2 -- the
-  exact result rounded to E4M3 already has a larger relative L2 error (the
-  "format floor"; e.g. outputs of a 65536-key flat softmax lie in E4M3's
-  subnormal range) -- the bound is 1.05 x that floor instead.
+  dequantisation (check_ctx).  The ulp distance is the difference of the
+  monotone code ordinals.  The "format floor" -- the relative L2 error of
+  the exact result rounded to E4M3, the best any E4M3 output can do -- is
+  printed beside it as a diagnostic only.
+* check_ctx_format_floor is a separate, weaker check for inputs whose exact
+  outputs lie among E4M3's subnormals (a 65536-key softmax at out_scale 1):
+  there the format alone misses 3e-2, so it asserts the ulp bar and a
+  relative L2 error within 1.05 x the floor, and says that 3e-2 is out of
+  reach.  No test of a stated configuration uses it in place of check_ctx.
 * Dequantisation: bit-exact.
 """
 import numpy as np
@@ -46,8 +50,7 @@ def e4m3_ordinal(codes):
     return np.where(c & 0x80, -mag, mag)
 
 
-def check_ctx(out_codes, ref, what=""):
-    """out_codes: uint8 E4M3 from the GPU; ref: fp64 exact O / out_scale."""
+def _ctx_measures(out_codes, ref):
     out_codes = np.asarray(out_codes, dtype=np.uint8)
     ref_codes = oracle.f64_to_e4m3(ref) if ref.size < 200000 else _fast_e4m3(ref)
     ulps = np.abs(e4m3_ordinal(out_codes) - e4m3_ordinal(ref_codes))
@@ -56,13 +59,31 @@ def check_ctx(out_codes, ref, what=""):
     got = table[out_codes]
     rl = rel_l2(got, ref)
     floor = rel_l2(table[ref_codes], ref)  # best any E4M3 output can do
-    bound = max(CTX_REL_L2, 1.05 * floor)
+    return got, ulps, frac, rl, floor
+
+
+def check_ctx(out_codes, ref, what=""):
+    """out_codes: uint8 E4M3 from the GPU; ref: fp64 exact O / out_scale.
+    Asserts the stated bar: >= 99.9 % within 2 ulps and rel-L2 <= 3e-2."""
+    got, ulps, frac, rl, floor = _ctx_measures(out_codes, ref)
     print(f"{what}: within {CTX_ULPS} ulps {frac:.6f} (max {int(ulps.max())}), rel-L2 {rl:.4e} "
-          f"(format floor {floor:.4e}, bound {bound:.4e})")
+          f"(bound {CTX_REL_L2:.1e}; E4M3 format floor {floor:.4e}, diagnostic)")
     assert np.isfinite(got).all(), f"{what}: NaN in output"
     assert frac >= CTX_FRAC_WITHIN, f"{what}: only {frac:.5f} within {CTX_ULPS} ulps (max {ulps.max()})"
-    assert rl <= bound, f"{what}: rel-L2 {rl:.3e} > {bound:.3e} (format floor {floor:.3e})"
+    assert rl <= CTX_REL_L2, f"{what}: rel-L2 {rl:.3e} > {CTX_REL_L2:.1e} (format floor {floor:.3e})"
     return frac, rl, int(ulps.max())
+
+
+def check_ctx_format_floor(out_codes, ref, what=""):
+    """The weaker check for outputs that E4M3 cannot hold to 3e-2 (see the
+    module docstring): the ulp bar, and rel-L2 within 1.05 x the floor."""
+    got, ulps, frac, rl, floor = _ctx_measures(out_codes, ref)
+    print(f"{what}: within {CTX_ULPS} ulps {frac:.6f} (max {int(ulps.max())}), rel-L2 {rl:.4e} against "
+          f"the format floor {floor:.4e}; the stated 3e-2 bound is {'met' if rl <= CTX_REL_L2 else 'NOT met'}")
+    assert np.isfinite(got).all(), f"{what}: NaN in output"
+    assert frac >= CTX_FRAC_WITHIN, f"{what}: only {frac:.5f} within {CTX_ULPS} ulps (max {ulps.max()})"
+    assert rl <= 1.05 * floor, f"{what}: rel-L2 {rl:.3e} > 1.05 x format floor {floor:.3e}"
+    return frac, rl, floor
 
 
 def _fast_e4m3(ref):
