@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "GqaError", "lib", "gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages",
-    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_paged", "gqa_debug_wait_expiry", "gqa_decode_noalloc", "LIB_PATH",
+    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_paged", "gqa_debug_wait_expiry", "gqa_decode_noalloc", "gqa_debug_starve_producers", "LIB_PATH",
     "build",
 ]
 
@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
             L.gqa_decode_paged.restype = c.c_int
             L.gqa_debug_wait_expiry.argtypes = [c.c_int, vp]
             L.gqa_debug_wait_expiry.restype = c.c_int
+            L.gqa_debug_starve_producers.argtypes = [c.c_int]
+            L.gqa_debug_starve_producers.restype = c.c_int
             L.gqa_release_workspace.argtypes = []
             L.gqa_release_workspace.restype = c.c_int
             _lib = L
@@ -246,6 +248,13 @@ def gqa_debug_wait_expiry(device: int = 0) -> None:
     import torch
     stream = torch.cuda.current_stream(device).cuda_stream
     _check(lib().gqa_debug_wait_expiry(int(device), ctypes.c_void_p(stream)))
+
+
+def gqa_debug_starve_producers(enable: bool) -> None:
+    """Test switch (see include/gqa.h): producers issue no copies, so every
+    consumer's bounded wait expires (~2 s); enable=False restores normal
+    operation."""
+    _check(lib().gqa_debug_starve_producers(1 if enable else 0))
 
 
 def gqa_check_device_errors(device: int = 0) -> int:

@@ -11,6 +11,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -171,13 +172,19 @@ struct Carver {
   }
 };
 
+std::atomic<int> g_starve{0};
+
 }  // namespace
+
+namespace gqa {
+int starve_producers() { return g_starve.load(std::memory_order_relaxed); }
+}  // namespace gqa
 
 extern "C" {
 
 const char* gqa_last_error(void) { return t_last_error.c_str(); }
 
-int gqa_version(void) { return 200; }  // 0.2.0: gqa_decode_paged, gqa_ctx_plan, split-KV context attention
+int gqa_version(void) { return 300; }  // 0.3.0: qo_indptr checked on the device, gqa_debug_starve_producers
 
 gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
                       int64_t capacity, float q_scale, gqa_stream_t stream_) {
@@ -398,6 +405,7 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
   if (st != GQA_OK) return st;
 
   gqa::CtxArgs a;
+  a.starve = gqa::starve_producers();
   a.q_scale = q_scale;
   a.out_scale = out_scale;
   a.batch = batch;
@@ -510,6 +518,11 @@ gqa_status gqa_debug_wait_expiry(int device, gqa_stream_t stream) {
   return GQA_OK;
 }
 
+gqa_status gqa_debug_starve_producers(int enable) {
+  g_starve.store(enable ? 1 : 0, std::memory_order_relaxed);
+  return GQA_OK;
+}
+
 gqa_status gqa_check_device_errors(int device, uint32_t* word) {
   if (!word) return fail(GQA_ERR_INVALID_ARG, "word is a null pointer");
   *word = 0;
@@ -520,7 +533,11 @@ gqa_status gqa_check_device_errors(int device, uint32_t* word) {
   GQA_CUDA_TRY(gqa::ctx_read_errors(&b), "read ctx error word");
   *word = a | b;
   if (*word & 1u) return fail(GQA_ERR_TIMEOUT, "a kernel's bounded wait expired (error word 0x%x)", *word);
-  if (*word) return fail(GQA_ERR_INVALID_ARG, "a kernel skipped out-of-range indices (error word 0x%x)", *word);
+  if (*word)
+    return fail(GQA_ERR_INVALID_ARG,
+                "a kernel met invalid metadata: bit 1 = out-of-range page index skipped, bit 2 = qo_indptr not "
+                "non-decreasing from 0 to total_q, bit 3 = dequantisation self-check (error word 0x%x)",
+                *word);
   return GQA_OK;
 }
 

@@ -1,13 +1,15 @@
 // common.cuh -- sm_103a device helpers shared by the libgqa kernels:
 // mbarrier rings with bounded waits, bulk (TMA) copies, a device error word.
 //
-// Every wait in this library is bounded: after ~kWaitNs nanoseconds of
-// polling, the waiting thread records an error code in the kernel's error
-// word and gives up, so a lost arrival degrades into a reported error
-// instead of a hung GPU.  No code path traps.
+// Every wait in this library is bounded: after kWaitNs (2 s) of polling, the
+// waiting thread records an error code in the kernel's error word and gives
+// up, so a lost arrival degrades into a reported error instead of a hung GPU.
+// No code path traps.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
+
+#include "kernels.h"  // kDefaultWaitNs
 
 namespace gqa {
 
@@ -19,9 +21,11 @@ constexpr int kPage = 64;      // tokens per NVFP4 page
 
 // Error codes written into a kernel's error word (bitwise OR).
 constexpr uint32_t kErrWaitTimeout = 1u;
-constexpr uint32_t kErrBadIndex = 2u;
+constexpr uint32_t kErrBadIndex = 2u;     // an out-of-range page index was skipped
+constexpr uint32_t kErrBadIndptr = 4u;    // qo_indptr is not non-decreasing from 0 to total_q
+constexpr uint32_t kErrSelfCheck = 8u;    // a debug export's internal cross-check failed
 
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kWaitNs = kDefaultWaitNs;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

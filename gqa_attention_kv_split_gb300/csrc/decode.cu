@@ -62,6 +62,15 @@ struct DecodeSmem {
   alignas(8) uint64_t empty[kStages];
 };
 
+// Producer epilogue: wait (bounded) until the copies of the last `issued`
+// stages have landed, so that none lands after the CTA has exited.  In a
+// normal run these phases completed long ago; after an expired wait the
+// consumers may have stopped before consuming them.
+__device__ __forceinline__ void drain_stages(DecodeSmem& sm, int issued) {
+  for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+    mbar_wait(smem_u32(&sm.full[i % kStages]), (i / kStages) & 1, &g_decode_err);
+}
+
 __device__ __forceinline__ void h8_to_f8(const uint4& u, float f[8]) {
   const __half2* h = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
@@ -79,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __half* __restrict__ q, const __half* __restrict__ kv, const DecodePages pages,
                         const int32_t* __restrict__ seq_lens, float* __restrict__ part_o,
                         float2* __restrict__ part_ml, __half* __restrict__ out, int64_t cap, int chunk,
-                        int n_splits, float scale_log2) {
+                        int n_splits, float scale_log2, const int starve) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
   const int s = blockIdx.x;
@@ -126,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     int nxt = 32 + lane < n_pg ? bt[32 + lane] : 0;
     const __half* kp = static_cast<const __half*>(pages.k_pages);
     const __half* vp = static_cast<const __half*>(pages.v_pages);
-    for (int i = 0; i < n_st; ++i) {
+    int issued = 0;
+    for (int i = 0; i < (starve ? 0 : n_st); ++i) {
       const int pi = i / (kPage / kStageTok);  // page of this stage within the chunk
       if (pi > 0 && (pi & 31) == 0 && i % (kPage / kStageTok) == 0) {
         cur = nxt;
@@ -150,8 +160,12 @@ __global__ void __launch_bounds__(kThreads, 3)
         bulk_g2s_hint(smem_u32(sm.k[st]), kp + off, bytes, fb, pol);
         bulk_g2s_hint(smem_u32(sm.v[st]), vp + off, bytes, fb, pol);
       }
+      issued = i + 1;
       __syncwarp();
     }
+    // No copy may land after the CTA exits (the consumers stop early when a
+    // wait expires): wait for the last issued stages.
+    if (lane == 0) drain_stages(sm, issued);
     return;
   }
   if (warp == kComputeWarps) {
@@ -160,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       const uint64_t pol = policy_evict_first();
       const __half* kbase = kv + (((int64_t)b * 2 + 0) * kHkv + g) * cap * kD + t0 * kD;
       const __half* vbase = kv + (((int64_t)b * 2 + 1) * kHkv + g) * cap * kD + t0 * kD;
-      for (int i = 0; i < n_st; ++i) {
+      int issued = 0;
+      for (int i = 0; i < (starve ? 0 : n_st); ++i) {
         const int st = i % kStages;
         if (i >= kStages && !mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1, &g_decode_err)) break;
         const int nt = min(kStageTok, n_tok - i * kStageTok);
@@ -169,7 +184,9 @@ __global__ void __launch_bounds__(kThreads, 3)
         mbar_arrive_expect_tx(fb, 2 * bytes);
         bulk_g2s_hint(smem_u32(sm.k[st]), kbase + (int64_t)i * kStageTok * kD, bytes, fb, pol);
         bulk_g2s_hint(smem_u32(sm.v[st]), vbase + (int64_t)i * kStageTok * kD, bytes, fb, pol);
+        issued = i + 1;
       }
+      drain_stages(sm, issued);
     }
     return;
   }
@@ -498,6 +515,7 @@ cudaError_t launch_decode_any(const void* q, const void* kv, const DecodePages* 
   if (e != cudaSuccess) return e;
   if ((e = ensure_smem_optin(dev)) != cudaSuccess) return e;
   const float scale_log2 = q_scale / sqrtf((float)kD) * 1.4426950408889634f;
+  const int starve = starve_producers();
   float* part_o = nullptr;
   float2* part_ml = nullptr;
   if (plan.n_splits > 1) {
@@ -509,11 +527,11 @@ cudaError_t launch_decode_any(const void* q, const void* kv, const DecodePages* 
   if (pages) {
     decode_split_kernel<true><<<grid, kThreads, sizeof(DecodeSmem), stream>>>(
         static_cast<const __half*>(q), nullptr, *pages, seq_lens, part_o, part_ml, static_cast<__half*>(out),
-        capacity, plan.chunk, plan.n_splits, scale_log2);
+        capacity, plan.chunk, plan.n_splits, scale_log2, starve);
   } else {
     decode_split_kernel<false><<<grid, kThreads, sizeof(DecodeSmem), stream>>>(
         static_cast<const __half*>(q), static_cast<const __half*>(kv), DecodePages{}, seq_lens, part_o, part_ml,
-        static_cast<__half*>(out), capacity, plan.chunk, plan.n_splits, scale_log2);
+        static_cast<__half*>(out), capacity, plan.chunk, plan.n_splits, scale_log2, starve);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (plan.n_splits > 1) {

@@ -7,6 +7,14 @@
 
 namespace gqa {
 
+// Limit of every bounded wait in the kernels: 2 s.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+// Process-wide test switch of the bounded-wait machinery (set by
+// gqa_debug_starve_producers): the kernels' producers issue no copies, so
+// every consumer's wait expires.
+int starve_producers();
+
 // ---- FP16 split-KV decode -------------------------------------------------
 
 struct DecodePlan {
@@ -81,6 +89,7 @@ struct CtxArgs {
   int64_t total_q;
   int64_t num_pages;
   int64_t max_pages_per_seq;
+  int starve;                  // test switch: the producer issues no copies
 };
 
 // Split-KV plan of the context attention, from host-known sizes only: when

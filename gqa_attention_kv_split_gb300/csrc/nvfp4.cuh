@@ -4,18 +4,24 @@
 // slot 조기 반납과 8단 packed K/V ring" (introduction) performs.
 //
 // value = E4M3_rne_satfinite( e2m1(code) * e4m3(scale) ).
-// The product is formed in f16, where it is exact: an E2M1 value has at most
-// 2 significant bits and an E4M3 value at most 4, every product lies within
-// [2^-10, 2688] in magnitude (or is zero), and f16 holds 11 significant bits
-// over [2^-14, 65504].  The single rounding is the hardware's f16x2 -> e4m3x2
-// conversion (round to nearest even, saturating to +-448).  Conversions run
-// at a fraction of the ALU rate on sm_103a, so the per-element work below is
-// byte permutes through a per-block table.
+// A 16-element block has one scale, so its 8 possible magnitudes are
+// tabulated once per scale: each product is formed in f16, where it is exact
+// (an E2M1 value has at most 2 significant bits and an E4M3 value at most 4;
+// every product lies within [2^-10, 2688] in magnitude or is zero, and f16
+// holds 11 significant bits over [2^-14, 65504]), and rounded once by the
+// hardware's f16x2 -> e4m3x2 conversion (round to nearest even, saturating to
+// +-448).  The per-element work is then byte permutes: the low 3 bits of a
+// code index the table of the 8 products and bit 3 (the E2M1 sign) flips the
+// sign bit of the result (a flip, not a set: the scale may be negative).
+//
+// Two outputs per code word: E4M3 bytes (the K tile of S = Q K^T) and the
+// same values widened to f16 (the V tile of the f16 P V product), the latter
+// looked up directly from a table of the f16 encodings of the E4M3 values,
+// so both are the same E4M3 numbers bit for bit.
 #pragma once
 #include <cstdint>
 
 namespace gqa {
-
 
 // E4M3 scale byte -> f16x2 (s, s).
 __device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t sf) {
@@ -38,25 +44,15 @@ __device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
   return r;
 }
 
-// One 16-element block: 8 packed bytes + its scale byte -> 16 E4M3 bytes.
-//
-// A block has one scale, so its 16 possible outputs are tabulated first: the
-// 8 E2M1 magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6} (f16x2 constants) times the
-// scale, rounded to E4M3 -- 4 products and 4 conversions per block instead of
-// 16 + 8.  Each group of 4 codes (16 bits, element order low nibble first)
-// then becomes 4 output bytes with two byte-permutes: the low 3 bits of each
-// nibble index the magnitude table, and bit 3 (the E2M1 sign) selects a
-// 0x80 byte that is XORed into the E4M3 sign.  Same values, bit for bit, as
-// converting every element: the products are exact in f16 and each is
-// rounded once, by the same conversion.
-__device__ __forceinline__ uint32_t nvfp4_lookup4(uint32_t codes16, uint32_t tab_lo, uint32_t tab_hi) {
-  const uint32_t mag = __byte_perm(tab_lo, tab_hi, codes16 & 0x7777u);
-  const uint32_t sgn = __byte_perm(0u, 0x80808080u, (codes16 >> 1) & 0x4444u);
-  return mag ^ sgn;
+// Two E4M3 bytes (low 16 bits, first element low) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"((uint16_t)v));
+  return d;
 }
 
-// The 8 E4M3 magnitudes of one scale: tab_lo = codes 0..3, tab_hi = codes
-// 4..7, one byte each (code c in byte c & 3).
+// The 8 E4M3 magnitudes of one scale: .x = codes 0..3, .y = codes 4..7, one
+// byte each (code c in byte c & 3).
 __device__ __forceinline__ uint2 nvfp4_scale_table(uint32_t sf_byte) {
   const uint32_t s = e4m3_to_f16x2_bcast(sf_byte);
   const uint32_t t01 = f16x2_to_e4m3x2(hmul2_u32(0x38000000u, s));  // (0, 0.5)
@@ -66,15 +62,50 @@ __device__ __forceinline__ uint2 nvfp4_scale_table(uint32_t sf_byte) {
   return make_uint2(t01 | (t23 << 16), t45 | (t67 << 16));
 }
 
-// One 16-element block through a scale table: 8 packed bytes -> 16 E4M3 bytes.
-__device__ __forceinline__ uint4 dequant16_table(uint2 packed, uint2 tab) {
-  return make_uint4(nvfp4_lookup4(packed.x & 0xffffu, tab.x, tab.y), nvfp4_lookup4(packed.x >> 16, tab.x, tab.y),
-                    nvfp4_lookup4(packed.y & 0xffffu, tab.x, tab.y), nvfp4_lookup4(packed.y >> 16, tab.x, tab.y));
+// The same 8 magnitudes as f16 encodings, split into byte tables: .x/.y =
+// low bytes of codes 0..3 / 4..7, .z/.w = high bytes.
+__device__ __forceinline__ uint4 nvfp4_f16_table(uint2 e4m3_tab) {
+  const uint32_t h01 = e4m3x2_to_f16x2(e4m3_tab.x & 0xffffu), h23 = e4m3x2_to_f16x2(e4m3_tab.x >> 16);
+  const uint32_t h45 = e4m3x2_to_f16x2(e4m3_tab.y & 0xffffu), h67 = e4m3x2_to_f16x2(e4m3_tab.y >> 16);
+  return make_uint4(__byte_perm(h01, h23, 0x6420), __byte_perm(h45, h67, 0x6420),
+                    __byte_perm(h01, h23, 0x7531), __byte_perm(h45, h67, 0x7531));
 }
 
-// One 16-element block: 8 packed bytes + its scale byte -> 16 E4M3 bytes.
-__device__ __forceinline__ uint4 dequant16(uint2 packed, uint32_t sf_byte) {
-  return dequant16_table(packed, nvfp4_scale_table(sf_byte));
+// Sign bits of 8 codes (a 32-bit word, code k in bits 4k..4k+3, element
+// order low nibble first) moved to bit 7 of output bytes: .x for codes 0..3,
+// .y for codes 4..7.  Code 2i's sign (bit 3 of byte i) reaches bit 7 of a
+// byte of w << 4; code 2i+1's sign already is bit 7 of byte i.
+__device__ __forceinline__ uint2 nvfp4_sign_bytes(uint32_t w) {
+  const uint32_t w4 = w << 4;
+  return make_uint2(__byte_perm(w4, w, 0x5140) & 0x80808080u, __byte_perm(w4, w, 0x7362) & 0x80808080u);
+}
+
+// 8 codes -> 8 E4M3 bytes (.x = elements 0..3, .y = 4..7).
+__device__ __forceinline__ uint2 nvfp4_to_e4m3_8(uint32_t w, uint2 tab) {
+  const uint32_t wm = w & 0x77777777u;  // magnitude indices (a selector nibble's bit 3 must be clear)
+  const uint2 sg = nvfp4_sign_bytes(w);
+  return make_uint2(__byte_perm(tab.x, tab.y, wm) ^ sg.x, __byte_perm(tab.x, tab.y, wm >> 16) ^ sg.y);
+}
+
+// 8 codes -> 8 f16 values of the E4M3 results, as 4 f16x2 words (element 2i
+// in the low half of word i).
+__device__ __forceinline__ uint4 nvfp4_to_f16_8(uint32_t w, uint4 tab) {
+  const uint32_t wm = w & 0x77777777u;
+  const uint32_t wmh = wm >> 16;
+  const uint2 sg = nvfp4_sign_bytes(w);
+  const uint32_t h0 = __byte_perm(tab.z, tab.w, wm) ^ sg.x;
+  const uint32_t h1 = __byte_perm(tab.z, tab.w, wmh) ^ sg.y;
+  const uint32_t l0 = __byte_perm(tab.x, tab.y, wm);
+  const uint32_t l1 = __byte_perm(tab.x, tab.y, wmh);
+  return make_uint4(__byte_perm(l0, h0, 0x5140), __byte_perm(l0, h0, 0x7362), __byte_perm(l1, h1, 0x5140),
+                    __byte_perm(l1, h1, 0x7362));
+}
+
+// One 16-element block (8 packed bytes) through its scale's table -> 16 E4M3 bytes.
+__device__ __forceinline__ uint4 dequant16_e4m3(uint2 packed, uint2 tab) {
+  const uint2 lo = nvfp4_to_e4m3_8(packed.x, tab);
+  const uint2 hi = nvfp4_to_e4m3_8(packed.y, tab);
+  return make_uint4(lo.x, lo.y, hi.x, hi.y);
 }
 
 }  // namespace gqa

@@ -199,7 +199,13 @@ gqa_status gqa_decode_plan(int64_t batch, int64_t capacity, int32_t* tokens_per_
  *   q_scale, out_scale  finite, out_scale > 0
  *
  * qo_indptr and kv_lens are read on the device only.  A query row that sees
- * no key (q_len_b > kv_len_b) is written as zeros.  The softmax numerators P
+ * no key (q_len_b > kv_len_b) is written as zeros.  The kernels check
+ * qo_indptr on the device: when it does not run non-decreasing from 0 to
+ * total_q they set bit 2 of the error word (gqa_check_device_errors), write
+ * rows past qo_indptr[batch] as zeros, and never read or write a row outside
+ * [0, total_q); the other rows are then unspecified.  (With host buffers the
+ * library checks qo_indptr, kv_lens and the used block-table entries before
+ * staging and returns GQA_ERR_INVALID_ARG.)  The softmax numerators P
  * enter the P*V product as f16 (V's dequantised E4M3 values widened to f16
  * exactly), so the result matches the exact value to within the output's
  * E4M3 rounding.
@@ -249,8 +255,13 @@ gqa_status gqa_debug_dequant_pages(const void* fp4, const void* sf, const int32_
 /*
  * gqa_check_device_errors -- synchronise `device` and return (then clear)
  * the kernels' device error word in *word: bit 0 = a bounded wait expired,
- * bit 1 = an out-of-range page index was skipped.  Returns GQA_ERR_TIMEOUT
- * when bit 0 is set, GQA_OK when the word is 0.
+ * bit 1 = an out-of-range page index was skipped, bit 2 = qo_indptr was not
+ * non-decreasing from 0 to total_q, bit 3 = the dequantisation export's
+ * self-check failed.  Returns GQA_ERR_TIMEOUT when bit 0 is set,
+ * GQA_ERR_INVALID_ARG when another bit is set, GQA_OK when the word is 0.
+ * After a timeout the outputs of the affected call are unspecified; every
+ * kernel waits for the tensor-core operations and copies it started before
+ * it releases its resources, so later calls are unaffected.
  */
 gqa_status gqa_check_device_errors(int device, uint32_t* word);
 
@@ -263,6 +274,17 @@ gqa_status gqa_check_device_errors(int device, uint32_t* word);
  * context stays usable.  Asynchronous on `stream`.
  */
 gqa_status gqa_debug_wait_expiry(int device, gqa_stream_t stream);
+
+/*
+ * gqa_debug_starve_producers -- test switch of the failure detection.  With
+ * enable != 0, every later launch (all devices, all threads) runs its
+ * kernels with producers that issue no copies: each consumer's bounded wait
+ * expires after about 2 s, every role leaves its loop, the CTA drains what it
+ * started, frees its tensor memory and exits, and gqa_check_device_errors
+ * reports GQA_ERR_TIMEOUT.  enable = 0 restores normal operation.  Not for
+ * concurrent use with real work: the setting is process-wide.
+ */
+gqa_status gqa_debug_starve_producers(int enable);
 
 /* Free every workspace the library holds (all devices and streams).  The
  * caller must ensure no libgqa work is still running. */

@@ -180,3 +180,8 @@ def test_ctx_plan_splits_only_small_calls():
     assert gqa.gqa_ctx_plan(1, 0, 16)["num_launches"] == 0
     with pytest.raises(gqa.GqaError):
         gqa.gqa_ctx_plan(0, 1, 16)
+
+
+def test_starvation_switch_toggles(L):
+    assert L.gqa_debug_starve_producers(1) == OK
+    assert L.gqa_debug_starve_producers(0) == OK  # off again (the default)

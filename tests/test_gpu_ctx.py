@@ -103,6 +103,71 @@ def test_many_sequences_and_empty_queries():
     check_ctx(run(x), ref(x), "40 sequences")
 
 
+def _call(x: W.CtxInputs, qo_indptr, out):
+    a = args_of(x)
+    gqa.nvfp4_paged_ctx_attn(*a[:6], qo_indptr.to(DEV), a[7], q_scale=x.q_scale, out_scale=x.out_scale, out=out)
+
+
+@pytest.mark.parametrize("q_lens,kv_lens", [([100, 60], [200, 60]), ([1, 2], [3000, 2000])])
+def test_short_qo_indptr_is_flagged_and_uncovered_rows_zeroed(q_lens, kv_lens):
+    """qo_indptr ending short of total_q (invalid metadata, checked on the
+    device): bit 2 of the error word, the rows past its last offset written
+    as zeros (by the attention kernel, or by the merge in split mode), and
+    the rows of the sequences before it still correct."""
+    x = W.make_ctx_inputs(q_lens, kv_lens, seed=56 + sum(kv_lens))
+    T = x.total_q
+    short = x.qo_indptr.clone()
+    short[-1] = short[-2] + 1  # last sequence keeps one row; the rest belong to no unit
+    out = torch.full((T, 32, 128), 0x55, dtype=torch.uint8, device=DEV)
+    _call(x, short, out)
+    assert gqa.gqa_check_device_errors(0) & 4
+    got = out.cpu().numpy()
+    last = int(short[-1])
+    assert np.all(got[last:] == 0)
+    keep = int(x.qo_indptr[-2])
+    check_ctx(got[:keep], ref(x)[:keep], f"rows before the short offset, q{q_lens}")
+
+
+def test_overlong_qo_indptr_writes_nothing_past_total_q():
+    """qo_indptr ending past total_q: flagged, and no row past total_q is
+    written (the output here is the head of a larger buffer)."""
+    x = W.make_ctx_inputs([70, 30], [100, 30], seed=58)
+    T = x.total_q
+    long = x.qo_indptr.clone()
+    long[-1] = T + 50
+    big = torch.full((T + 64, 32, 128), 0x55, dtype=torch.uint8, device=DEV)
+    _call(x, long, big[:T])
+    assert gqa.gqa_check_device_errors(0) & 4
+    assert bool((big[T:] == 0x55).all())
+
+
+def test_bounded_waits_expire_in_the_context_kernels():
+    """Failure detection in the real kernels: with the producers starved (no
+    copy issued) every role's wait expires, the
+    CTAs drain and free their tensor memory, the host reads GQA_ERR_TIMEOUT,
+    and the next normal calls -- unsplit and split -- are correct."""
+    import time
+    x = W.make_ctx_inputs([100, 40], [300, 40], seed=57)
+    xs = W.make_ctx_inputs([1, 3], [1100, 900], seed=22)
+    assert plan_of(x)["num_splits"] == 1 and plan_of(xs)["num_splits"] > 1
+    assert gqa.gqa_check_device_errors(0) == 0
+    words = []
+    gqa.gqa_debug_starve_producers(True)
+    try:
+        t0 = time.perf_counter()
+        for case in (x, xs):
+            gqa.nvfp4_paged_ctx_attn(*args_of(case), q_scale=case.q_scale, out_scale=case.out_scale)
+            words.append(gqa.gqa_check_device_errors(0))
+        took = time.perf_counter() - t0
+    finally:
+        gqa.gqa_debug_starve_producers(False)
+    assert all(w & 1 for w in words), words
+    assert took < 60
+    check_ctx(run(x), ref(x), "unsplit, after expired waits")
+    check_ctx(run(xs), ref(xs), "split, after expired waits")
+    assert gqa.gqa_check_device_errors(0) == 0
+
+
 def plan_of(x: W.CtxInputs):
     return gqa.gqa_ctx_plan(x.block_table.shape[0], x.q_fp8.shape[0], x.block_table.shape[1])
 

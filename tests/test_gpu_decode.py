@@ -203,6 +203,36 @@ def test_paged_decode_host_path_checks_the_table():
         gqa.gqa_decode_paged(q, pages, pages, bt, torch.tensor([100], dtype=torch.int32))
 
 
+def test_bounded_waits_expire_in_the_decode_kernels():
+    """Failure detection in the real kernels: producers starved (each wait
+    expires after ~2 s); the stacked and the paged decode (split + merge, and a single
+    split) report GQA_ERR_TIMEOUT, and the next normal calls are correct."""
+    import time
+    x = W.make_decode_inputs(4, 4096, [4096, 100, 0, 3000], seed=14)
+    x1 = W.make_decode_inputs(2, 256, [1, 200], seed=15)
+    p = W.page_decode_inputs(x, seed=14)
+    assert gqa.gqa_decode_plan(4, 4096)["num_launches"] == 2 and gqa.gqa_decode_plan(2, 256)["num_launches"] == 1
+    assert gqa.gqa_check_device_errors(0) == 0
+    words = []
+    gqa.gqa_debug_starve_producers(True)
+    try:
+        t0 = time.perf_counter()
+        for case in (x, x1):
+            gqa.gqa_decode(case.q.to(DEV), case.kv.to(DEV), case.seq_lens.to(DEV), q_scale=case.q_scale)
+            words.append(gqa.gqa_check_device_errors(0))
+        run_paged(p)
+        words.append(gqa.gqa_check_device_errors(0))
+        took = time.perf_counter() - t0
+    finally:
+        gqa.gqa_debug_starve_producers(False)
+    assert all(w & 1 for w in words), words
+    assert took < 60
+    check_decode(run(x).double().numpy(), ref(x), "decode after expired waits")
+    check_decode(run(x1).double().numpy(), ref(x1), "single split after expired waits")
+    check_decode(run_paged(p).double().numpy(), ref_paged(p), "paged decode after expired waits")
+    assert gqa.gqa_check_device_errors(0) == 0
+
+
 def test_bounded_wait_expires_and_is_reported():
     """Failure detection without a fault: a wait that nothing completes gives
     up after ~2 s, the host reads GQA_ERR_TIMEOUT (bit 0), and the context is

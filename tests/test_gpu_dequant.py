@@ -1,5 +1,8 @@
 """The context kernel's NVFP4 -> E4M3 dequantisation, bit-exact against the
-oracle's decoded E4M3 tiles, through gqa_debug_dequant_pages."""
+oracle's decoded E4M3 tiles, through gqa_debug_dequant_pages.  The export
+writes the K path's E4M3 bytes and checks on the device that the V path's
+f16 values are the same numbers (bit 3 of the error word otherwise), so a
+clean error word after the bit-exact comparison covers both paths."""
 import numpy as np
 import pytest
 import torch
@@ -25,6 +28,7 @@ def test_random_pages_bit_exact(shuffle):
         got = gpu_dequant(fp4, sf, x.block_table, x.kv_lens, 200)
         exp = oracle.dequant_pages(fp4.numpy(), sf.numpy(), x.block_table.numpy(), x.kv_lens.numpy(), 200)
         assert np.array_equal(got, exp)
+    assert gqa.gqa_check_device_errors(0) == 0
 
 
 def test_every_code_and_scale_bit_exact():
@@ -47,3 +51,4 @@ def test_every_code_and_scale_bit_exact():
     exp = oracle.dequant_pages(fp4.numpy(), sf.numpy(), bt.numpy(), kl.numpy(), n_tok)
     bad = np.argwhere(got != exp)
     assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+    assert gqa.gqa_check_device_errors(0) == 0  # the V path's f16 values agreed with every E4M3 byte
