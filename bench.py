@@ -27,6 +27,10 @@ generator, the recipe of gqa_workloads) and resident in HBM before timing.
 --impl reference times the fp64 CPU oracle instead (the reference arm): each
 step is a bounded sample of the headline workload on the host cores.
 --workload NAME benchmarks a single named workload (see gqa_workloads).
+--study times every instantiated ring-depth schedule (gqa_set_schedule)
+against the production depths on the context and decode workloads,
+interleaved, L2 flushed before each call, and checks that every schedule's
+output is byte-identical to the production one.
 
 Multi-GPU: `--gpus N` under torchrun runs N independent replicas (the path
 has no exchange step); value = bytes all ranks processed / max time.
@@ -546,6 +550,66 @@ def run_gpu(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- ring-depth study --
+
+def run_study(args):
+    """One JSON line: per workload and schedule, the median of interleaved
+    event-timed calls and whether the output is byte-identical to the
+    production depths'."""
+    import torch
+
+    import gqa_attention_kv_split_gb300 as gqa
+    import gqa_workloads as W
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    gqa.lib()
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(torch, dev)
+    names = [args.workload] if args.workload else ["ctx_b2_q4096_kv65536", "ctx_b4_q2048_kv2048",
+                                                   "decode_b8_cap131072", "decode_b64_cap8192"]
+    rows = []
+    with ClockSampler(0) as clk:
+        time.sleep(0.3)
+        clk.mark("start")
+        for name in names:
+            wl = Workload(gqa, W, name, dev)
+            if wl.kind == "ctx":
+                scheds = [(st, sl, 0) for st, sl in gqa.CTX_SCHEDULES]
+            else:
+                scheds = [(0, 0, d) for d in gqa.DECODE_SCHEDULES]
+            outs, evs = {}, {sc: [] for sc in scheds}
+            for sc in scheds:  # warm-up and the output of every schedule
+                gqa.gqa_set_schedule(*sc)
+                for _ in range(3):
+                    wl.call()
+                torch.cuda.synchronize()
+                outs[sc] = wl.out.clone()
+            reps = 20 if name == "ctx_b2_q4096_kv65536" else 100
+            for _ in range(reps):
+                for sc in scheds:
+                    gqa.gqa_set_schedule(*sc)
+                    flush()
+                    a, b = _events(torch, 2)
+                    a.record(stream)
+                    wl.call()
+                    b.record(stream)
+                    evs[sc].append((a, b))
+            torch.cuda.synchronize()
+            gqa.gqa_set_schedule(0, 0, 0)
+            base = None
+            for sc in scheds:
+                ms = statistics.median(a.elapsed_time(b) for a, b in evs[sc])
+                base = base or ms
+                rows.append({"workload": name, "ctx_packed_stages": sc[0] or None, "ctx_kv_slots": sc[1] or None,
+                             "decode_stages": sc[2] or None, "ms_median": round(ms, 5),
+                             "value": round(wl.rate(ms), 2), "unit": wl.unit, "speed_vs_production": round(base / ms, 4),
+                             "byte_identical": bool(torch.equal(outs[sc], outs[scheds[0]])), "reps": reps})
+            del wl
+            torch.cuda.empty_cache()
+        clk.mark("stop")
+    print(json.dumps({"study": "ring depths (gqa_set_schedule)", "rows": rows, "clocks": clk.summary()}), flush=True)
+
+
 # ---------------------------------------------------------- oracle (CPU) --
 
 def _decode_sample(dx, n_seq):
@@ -738,6 +802,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=6.0, help="seconds of oracle time per configuration")
     ap.add_argument("--ref-seqs", type=int, default=0, help="reference arm: sequences per step (decode)")
     ap.add_argument("--ref-rows", type=int, default=0, help="reference arm: (row, head) items per step (ctx)")
+    ap.add_argument("--study", action="store_true",
+                    help="time every instantiated ring-depth schedule against the production depths and exit")
     ap.add_argument("--peaks", action="store_true",
                     help="measure context peaks (read-only HBM stream, bf16 and FP8 GEMMs) and exit")
     args = ap.parse_args(argv)
@@ -749,6 +815,9 @@ def main(argv=None):
             clk.mark("stop")
         res["clocks"] = clk.summary()
         print(json.dumps(res))
+        return
+    if args.study:
+        run_study(args)
         return
     if args.warmup < 3 and args.impl == "ours":
         print("note: warm-up raised to the minimum of 3 steps", file=sys.stderr)

@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "GqaError", "lib", "gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages",
-    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_paged", "gqa_debug_wait_expiry", "gqa_decode_noalloc", "gqa_debug_starve_producers", "LIB_PATH",
+    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_paged", "gqa_debug_wait_expiry", "gqa_decode_noalloc", "gqa_debug_starve_producers", "gqa_set_schedule", "LIB_PATH",
     "build",
 ]
 
@@ -84,6 +84,9 @@ def lib() -> ctypes.CDLL:
             L.gqa_debug_wait_expiry.argtypes = [c.c_int, vp]
             L.gqa_debug_wait_expiry.restype = c.c_int
             L.gqa_debug_starve_producers.argtypes = [c.c_int]
+            L.gqa_debug_starve_producers.restype = c.c_int
+            L.gqa_set_schedule.argtypes = [c.c_int, c.c_int, c.c_int]
+            L.gqa_set_schedule.restype = c.c_int
             L.gqa_debug_starve_producers.restype = c.c_int
             L.gqa_release_workspace.argtypes = []
             L.gqa_release_workspace.restype = c.c_int
@@ -255,6 +258,16 @@ def gqa_debug_starve_producers(enable: bool) -> None:
     consumer's bounded wait expires (~2 s); enable=False restores normal
     operation."""
     _check(lib().gqa_debug_starve_producers(1 if enable else 0))
+
+
+def gqa_set_schedule(ctx_packed_stages: int = 0, ctx_kv_slots: int = 0, decode_stages: int = 0) -> None:
+    """Study switch (see include/gqa.h): ring depths of later launches; 0 =
+    production depth.  Raises GqaError for a depth that is not instantiated."""
+    _check(lib().gqa_set_schedule(int(ctx_packed_stages), int(ctx_kv_slots), int(decode_stages)))
+
+
+CTX_SCHEDULES = [(6, 4), (4, 4), (8, 4), (10, 4), (6, 3), (12, 3), (6, 5), (6, 2)]
+DECODE_SCHEDULES = [8, 4, 12, 16]
 
 
 def gqa_check_device_errors(device: int = 0) -> int:

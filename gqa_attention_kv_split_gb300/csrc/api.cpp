@@ -173,11 +173,15 @@ struct Carver {
 };
 
 std::atomic<int> g_starve{0};
+std::atomic<int> g_ctx_stages{0}, g_ctx_slots{0}, g_decode_stages{0};
 
 }  // namespace
 
 namespace gqa {
 int starve_producers() { return g_starve.load(std::memory_order_relaxed); }
+int schedule_ctx_stages() { return g_ctx_stages.load(std::memory_order_relaxed); }
+int schedule_ctx_slots() { return g_ctx_slots.load(std::memory_order_relaxed); }
+int schedule_decode_stages() { return g_decode_stages.load(std::memory_order_relaxed); }
 }  // namespace gqa
 
 extern "C" {
@@ -518,6 +522,19 @@ gqa_status gqa_debug_wait_expiry(int device, gqa_stream_t stream) {
   return GQA_OK;
 }
 
+gqa_status gqa_set_schedule(int ctx_packed_stages, int ctx_kv_slots, int decode_stages) {
+  if (!gqa::ctx_schedule_supported(ctx_packed_stages, ctx_kv_slots))
+    return fail(GQA_ERR_UNSUPPORTED,
+                "context ring depths (%d packed stages, %d K/V slots) are not instantiated; see gqa.h", ctx_packed_stages,
+                ctx_kv_slots);
+  if (!gqa::decode_schedule_supported(decode_stages))
+    return fail(GQA_ERR_UNSUPPORTED, "decode ring depth %d is not instantiated (0, 4, 8, 12 or 16)", decode_stages);
+  g_ctx_stages.store(ctx_packed_stages, std::memory_order_relaxed);
+  g_ctx_slots.store(ctx_kv_slots, std::memory_order_relaxed);
+  g_decode_stages.store(decode_stages, std::memory_order_relaxed);
+  return GQA_OK;
+}
+
 gqa_status gqa_debug_starve_producers(int enable) {
   g_starve.store(enable ? 1 : 0, std::memory_order_relaxed);
   return GQA_OK;
@@ -528,10 +545,11 @@ gqa_status gqa_check_device_errors(int device, uint32_t* word) {
   *word = 0;
   ScopedDevice sd(device);
   if (!sd.ok()) return fail(GQA_ERR_CUDA, "cannot switch to device %d", device);
-  uint32_t a = 0, b = 0;
+  uint32_t a = 0, b = 0, c = 0;
   GQA_CUDA_TRY(gqa::decode_read_errors(&a), "read decode error word");
   GQA_CUDA_TRY(gqa::ctx_read_errors(&b), "read ctx error word");
-  *word = a | b;
+  GQA_CUDA_TRY(gqa::ctx_study_read_errors(&c), "read ctx study error word");
+  *word = a | b | c;
   if (*word & 1u) return fail(GQA_ERR_TIMEOUT, "a kernel's bounded wait expired (error word 0x%x)", *word);
   if (*word)
     return fail(GQA_ERR_INVALID_ARG,

@@ -58,6 +58,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <type_traits>
 
@@ -135,7 +136,7 @@ __device__ __forceinline__ int q_len_of(const int32_t* __restrict__ qo, int b, i
 // round r every sequence with more than r query blocks contributes its block
 // (n_blocks - 1 - r), in batch order.  All lanes of the calling warp get the
 // same answer; b = -1 when t is past the last unit.
-__device__ void find_unit(const int32_t* __restrict__ qo, int B, int64_t total_q, int t, int& out_b,
+static __device__ void find_unit(const int32_t* __restrict__ qo, int B, int64_t total_q, int t, int& out_b,
                           int& out_qb) {
   const int lane = threadIdx.x & 31;
   out_b = -1;
@@ -787,6 +788,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_thread_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Launch of one instance of the attention kernel; the dynamic-shared-memory
+// opt-in is made once per device and instance (cached bitmask).  (Internal
+// linkage: every translation unit that launches an instance owns it, and its
+// error word.)
+template <bool kSplit, int kNP, int kNK>
+static cudaError_t launch_attention(const CtxArgs& a, const CUtensorMap& q_map, dim3 grid, float scale_log2,
+                                    float inv_out_scale, int tiles_per_split, float* part_o, float2* part_ml,
+                                    cudaStream_t stream) {
+  static std::atomic<uint64_t> ready{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  constexpr size_t smem = smem_bytes<kNP, kNK>();
+  static_assert(smem <= 232448, "shared memory of this ring depth exceeds the per-block maximum");
+  if (!(ready.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(ctx_nvfp4_kernel<kSplit, kNP, kNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    ready.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  ctx_nvfp4_kernel<kSplit, kNP, kNK><<<grid, kThreads, smem, stream>>>(a, q_map, scale_log2, inv_out_scale,
+                                                                       tiles_per_split, part_o, part_ml);
+  return cudaGetLastError();
+}
+
+// Reads and clears this translation unit's error word (synchronises the device).
+static cudaError_t read_ctx_error_word(uint32_t* word) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  uint32_t zero = 0;
+  if ((e = cudaMemcpyFromSymbol(word, g_ctx_err, sizeof(uint32_t))) != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_ctx_err, &zero, sizeof(uint32_t));
 }
 
 }  // namespace ctx

@@ -1,6 +1,7 @@
 // ctx_nvfp4.cu -- host side of the NVFP4 paged context attention for
 // sm_103a: split-KV planning, launch of the attention kernel (ctx_kernel.cuh)
-// and of its split-KV merge, and the test export of the dequantisation.
+// at the production ring depths and of its split-KV merge, and the test
+// export of the dequantisation.  (Other ring depths: ctx_study.cu.)
 //
 // Operation ("GB300 NVFP4 Context Attention: scale slot 조기 반납과 8단 packed
 // K/V ring", introduction): see ctx_kernel.cuh.
@@ -119,29 +120,6 @@ __global__ void __launch_bounds__(32 * kMergeWarps)
   reinterpret_cast<uint32_t*>(out + row * kD)[lane] = f4_to_e4m3x4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-// Launch of one instance of the attention kernel; the dynamic-shared-memory
-// opt-in is made once per device and instance (cached bitmask).
-template <bool kSplit, int kNP, int kNK>
-cudaError_t launch_attention(const CtxArgs& a, const CUtensorMap& q_map, dim3 grid, float scale_log2,
-                             float inv_out_scale, int tiles_per_split, float* part_o, float2* part_ml,
-                             cudaStream_t stream) {
-  static std::atomic<uint64_t> ready{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  constexpr size_t smem = smem_bytes<kNP, kNK>();
-  if (!(ready.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(ctx_nvfp4_kernel<kSplit, kNP, kNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    ready.fetch_or(bit, std::memory_order_acq_rel);
-  }
-  ctx_nvfp4_kernel<kSplit, kNP, kNK><<<grid, kThreads, smem, stream>>>(a, q_map, scale_log2, inv_out_scale,
-                                                                       tiles_per_split, part_o, part_ml);
-  return cudaGetLastError();
-}
-
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -217,9 +195,14 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
   alignas(64) CUtensorMap q_map;
   cudaError_t e = make_q_map(a.q, a.total_q, &q_map);
   if (e != cudaSuccess) return e;
-  if (plan.n_splits <= 1)
+  if (plan.n_splits <= 1) {
+    const int st = schedule_ctx_stages(), sl = schedule_ctx_slots();
+    if ((st && st != kCtxStagesDefault) || (sl && sl != kCtxSlotsDefault))
+      return launch_ctx_study(a, q_map, (unsigned)grid, scale_log2, inv_out_scale, st ? st : kCtxStagesDefault,
+                              sl ? sl : kCtxSlotsDefault, stream);
     return launch_attention<false, kCtxStagesDefault, kCtxSlotsDefault>(
         a, q_map, dim3((unsigned)grid, 1), scale_log2, inv_out_scale, 0, nullptr, nullptr, stream);
+  }
   // the merge holds one range per lane
   if (!workspace || plan.tiles_per_split < 1 || plan.n_splits > 32) return cudaErrorInvalidValue;
   const int64_t rows = a.total_q * kHq;
@@ -247,12 +230,6 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
                             plan.n_splits, inv_out_scale, a.qo_indptr, a.batch);
 }
 
-cudaError_t ctx_read_errors(uint32_t* word) {
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return e;
-  uint32_t zero = 0;
-  if ((e = cudaMemcpyFromSymbol(word, g_ctx_err, sizeof(uint32_t))) != cudaSuccess) return e;
-  return cudaMemcpyToSymbol(g_ctx_err, &zero, sizeof(uint32_t));
-}
+cudaError_t ctx_read_errors(uint32_t* word) { return read_ctx_error_word(word); }
 
 }  // namespace gqa

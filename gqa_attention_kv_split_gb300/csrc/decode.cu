@@ -38,7 +38,7 @@ namespace gqa {
 namespace {
 
 constexpr int kStageTok = 16;                         // tokens per ring stage
-constexpr int kStages = 8;                            // ring depth
+constexpr int kStagesDefault = 8;                     // ring depth of the production instances
 constexpr int kComputeWarps = 4;                      // consumer warps
 constexpr int kThreads = (kComputeWarps + 1) * 32;    // + one producer warp
 constexpr int kRowBytes = kD * 2;                     // one token of one head: 256 B
@@ -46,11 +46,12 @@ constexpr int kStageBytes = kStageTok * kRowBytes;    // 4 KB of K (and of V)
 constexpr int kChunkQuantum = kStageTok * kComputeWarps;  // 64 tokens
 // Consumer warp w takes ring positions w, w + kComputeWarps, ...; with a ring
 // depth that is a multiple of the warp count every stage belongs to one warp,
-// so no warp can wait on a stage's barrier a phase ahead of the data.
-static_assert(kStages % kComputeWarps == 0, "each ring stage must be owned by one consumer warp");
+// so no warp can wait on a stage's barrier a phase ahead of the data (checked
+// in the kernel template for every depth instantiated).
 
 __device__ uint32_t g_decode_err;
 
+template <int kStages>
 struct DecodeSmem {
   alignas(1024) uint8_t k[kStages][kStageBytes];
   alignas(128) uint8_t v[kStages][kStageBytes];
@@ -66,7 +67,8 @@ struct DecodeSmem {
 // stages have landed, so that none lands after the CTA has exited.  In a
 // normal run these phases completed long ago; after an expired wait the
 // consumers may have stopped before consuming them.
-__device__ __forceinline__ void drain_stages(DecodeSmem& sm, int issued) {
+template <int kStages>
+__device__ __forceinline__ void drain_stages(DecodeSmem<kStages>& sm, int issued) {
   for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
     mbar_wait(smem_u32(&sm.full[i % kStages]), (i / kStages) & 1, &g_decode_err);
 }
@@ -83,14 +85,15 @@ __device__ __forceinline__ void h8_to_f8(const uint4& u, float f[8]) {
 
 // kPaged: K/V come from 64-token HND pages through a block table (pages;
 // kv unused); otherwise from the stacked cache kv [B, 2, 8, cap, 128].
-template <bool kPaged>
+template <bool kPaged, int kStages>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __half* __restrict__ q, const __half* __restrict__ kv, const DecodePages pages,
                         const int32_t* __restrict__ seq_lens, float* __restrict__ part_o,
                         float2* __restrict__ part_ml, __half* __restrict__ out, int64_t cap, int chunk,
                         int n_splits, float scale_log2, const int starve) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  static_assert(kStages % kComputeWarps == 0, "each ring stage must be owned by one consumer warp");
+  DecodeSmem<kStages>& sm = *reinterpret_cast<DecodeSmem<kStages>*>(smem_raw);
   const int s = blockIdx.x;
   const int g = blockIdx.y;
   const int b = blockIdx.z;
@@ -465,22 +468,34 @@ __global__ void __launch_bounds__(128)
   reinterpret_cast<uint2*>(out + row * kD)[lane] = pk;
 }
 
-std::atomic<uint64_t> g_smem_ready{0};  // per-device bit: smem opt-in done
-
-cudaError_t ensure_smem_optin(int dev) {
+// Launch of one instance of the split kernel; the dynamic-shared-memory
+// opt-in is made once per device and instance (cached bitmask).
+template <bool kPaged, int kStages>
+cudaError_t launch_split(dim3 grid, cudaStream_t stream, const __half* q, const __half* kv, const DecodePages& pages,
+                         const int32_t* seq_lens, float* part_o, float2* part_ml, __half* out, int64_t cap, int chunk,
+                         int n_splits, float scale_log2, int starve) {
+  static std::atomic<uint64_t> ready{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
-  if (g_smem_ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)sizeof(DecodeSmem));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sizeof(DecodeSmem));
-  if (e != cudaSuccess) return e;
-  g_smem_ready.fetch_or(bit, std::memory_order_acq_rel);
-  return cudaSuccess;
+  constexpr size_t smem = sizeof(DecodeSmem<kStages>);
+  if (!(ready.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(decode_split_kernel<kPaged, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    ready.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  decode_split_kernel<kPaged, kStages><<<grid, kThreads, smem, stream>>>(q, kv, pages, seq_lens, part_o, part_ml,
+                                                                        out, cap, chunk, n_splits, scale_log2, starve);
+  return cudaGetLastError();
 }
 
 }  // namespace
+
+bool decode_schedule_supported(int stages) {
+  return stages == 0 || stages == 4 || stages == kStagesDefault || stages == 12 || stages == 16;
+}
 
 DecodePlan plan_decode(int64_t batch, int64_t capacity) {
   DecodePlan p;
@@ -510,10 +525,7 @@ namespace {
 cudaError_t launch_decode_any(const void* q, const void* kv, const DecodePages* pages, const int32_t* seq_lens,
                               void* out, int64_t batch, int64_t capacity, float q_scale, const DecodePlan& plan,
                               void* workspace, cudaStream_t stream) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_optin(dev)) != cudaSuccess) return e;
+  cudaError_t e;
   const float scale_log2 = q_scale / sqrtf((float)kD) * 1.4426950408889634f;
   const int starve = starve_producers();
   float* part_o = nullptr;
@@ -524,16 +536,34 @@ cudaError_t launch_decode_any(const void* q, const void* kv, const DecodePages* 
     part_ml = reinterpret_cast<float2*>(part_o + rows * kD);
   }
   dim3 grid((unsigned)plan.n_splits, kHkv, (unsigned)batch);
+  const __half* qh = static_cast<const __half*>(q);
+  __half* oh = static_cast<__half*>(out);
   if (pages) {
-    decode_split_kernel<true><<<grid, kThreads, sizeof(DecodeSmem), stream>>>(
-        static_cast<const __half*>(q), nullptr, *pages, seq_lens, part_o, part_ml, static_cast<__half*>(out),
-        capacity, plan.chunk, plan.n_splits, scale_log2, starve);
+    e = launch_split<true, kStagesDefault>(grid, stream, qh, nullptr, *pages, seq_lens, part_o, part_ml, oh, capacity,
+                                           plan.chunk, plan.n_splits, scale_log2, starve);
   } else {
-    decode_split_kernel<false><<<grid, kThreads, sizeof(DecodeSmem), stream>>>(
-        static_cast<const __half*>(q), static_cast<const __half*>(kv), DecodePages{}, seq_lens, part_o, part_ml,
-        static_cast<__half*>(out), capacity, plan.chunk, plan.n_splits, scale_log2, starve);
+    const __half* kvh = static_cast<const __half*>(kv);
+    const DecodePages none{};
+    // ring depth: the production depth, or another instantiated depth chosen for a study (gqa_set_schedule)
+    switch (schedule_decode_stages()) {
+      case 4:
+        e = launch_split<false, 4>(grid, stream, qh, kvh, none, seq_lens, part_o, part_ml, oh, capacity, plan.chunk,
+                                   plan.n_splits, scale_log2, starve);
+        break;
+      case 12:
+        e = launch_split<false, 12>(grid, stream, qh, kvh, none, seq_lens, part_o, part_ml, oh, capacity, plan.chunk,
+                                    plan.n_splits, scale_log2, starve);
+        break;
+      case 16:
+        e = launch_split<false, 16>(grid, stream, qh, kvh, none, seq_lens, part_o, part_ml, oh, capacity, plan.chunk,
+                                    plan.n_splits, scale_log2, starve);
+        break;
+      default:
+        e = launch_split<false, kStagesDefault>(grid, stream, qh, kvh, none, seq_lens, part_o, part_ml, oh, capacity,
+                                                plan.chunk, plan.n_splits, scale_log2, starve);
+    }
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   if (plan.n_splits > 1) {
     // programmatic dependent launch: the merge's launch and its seq_lens read
     // overlap the split kernel's last CTAs (griddepcontrol.wait orders the rest)

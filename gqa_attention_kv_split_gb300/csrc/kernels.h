@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap
 #include <cuda_runtime.h>
 
 namespace gqa {
@@ -14,6 +15,15 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 // gqa_debug_starve_producers): the kernels' producers issue no copies, so
 // every consumer's wait expires.
 int starve_producers();
+
+// Ring depths used by the next launches (set by gqa_set_schedule for
+// studies; 0 = the production depth).  Only the instantiated depths are
+// accepted: see gqa_set_schedule in include/gqa.h.
+int schedule_ctx_stages();
+int schedule_ctx_slots();
+int schedule_decode_stages();
+bool ctx_schedule_supported(int stages, int slots);
+bool decode_schedule_supported(int stages);
 
 // ---- FP16 split-KV decode -------------------------------------------------
 
@@ -115,5 +125,12 @@ cudaError_t launch_dequant_pages(const uint8_t* fp4, const uint8_t* sf, const in
                                  int64_t max_pages_per_seq, int64_t max_kv, cudaStream_t stream);
 
 cudaError_t ctx_read_errors(uint32_t* word);
+
+// The unsplit attention kernel at ring depths other than the production ones
+// (a separate translation unit); cudaErrorNotSupported for a combination that
+// is not instantiated.
+cudaError_t launch_ctx_study(const CtxArgs& a, const CUtensorMap& q_map, unsigned grid, float scale_log2,
+                             float inv_out_scale, int stages, int slots, cudaStream_t stream);
+cudaError_t ctx_study_read_errors(uint32_t* word);
 
 }  // namespace gqa

@@ -276,6 +276,26 @@ gqa_status gqa_check_device_errors(int device, uint32_t* word);
 gqa_status gqa_debug_wait_expiry(int device, gqa_stream_t stream);
 
 /*
+ * gqa_set_schedule -- study switch: ring depths of later launches (all
+ * devices, all threads; process-wide).  Every depth computes the same
+ * result, bit for bit -- the invariant "GB300 NVFP4 Context Attention: scale
+ * slot 조기 반납과 8단 packed K/V ring" checks for its ring changes (section 2
+ * and its results section) -- so a schedule changes only speed.
+ *
+ *   ctx_packed_stages, ctx_kv_slots  packed NVFP4 page stages and dequantised
+ *       K/V tile slots of the (unsplit) context attention kernel; 0 = the
+ *       production depth (6 stages, 4 slots).  Instantiated (stages, slots):
+ *       (6,4) (4,4) (8,4) (10,4) (6,3) (12,3) (6,5) (6,2).  Split-KV calls
+ *       always run the production depths.
+ *   decode_stages  16-token K/V stages of the decode ring (stacked cache);
+ *       0 = the production depth 8; also 4, 12, 16.  The paged decode always
+ *       runs depth 8.
+ *
+ * GQA_ERR_UNSUPPORTED for a depth that is not instantiated (nothing changes).
+ */
+gqa_status gqa_set_schedule(int ctx_packed_stages, int ctx_kv_slots, int decode_stages);
+
+/*
  * gqa_debug_starve_producers -- test switch of the failure detection.  With
  * enable != 0, every later launch (all devices, all threads) runs its
  * kernels with producers that issue no copies: each consumer's bounded wait

@@ -185,3 +185,14 @@ def test_ctx_plan_splits_only_small_calls():
 def test_starvation_switch_toggles(L):
     assert L.gqa_debug_starve_producers(1) == OK
     assert L.gqa_debug_starve_producers(0) == OK  # off again (the default)
+
+
+def test_schedule_switch_accepts_only_instantiated_depths(L):
+    for st, sl in gqa.CTX_SCHEDULES:
+        assert L.gqa_set_schedule(st, sl, 0) == OK
+    for d in gqa.DECODE_SCHEDULES:
+        assert L.gqa_set_schedule(0, 0, d) == OK
+    assert L.gqa_set_schedule(7, 4, 0) == UNSUPPORTED
+    assert b"not instantiated" in L.gqa_last_error()
+    assert L.gqa_set_schedule(0, 0, 6) == UNSUPPORTED  # not a multiple of the 4 consumer warps
+    assert L.gqa_set_schedule(0, 0, 0) == OK  # production depths again
