@@ -196,3 +196,12 @@ def test_schedule_switch_accepts_only_instantiated_depths(L):
     assert b"not instantiated" in L.gqa_last_error()
     assert L.gqa_set_schedule(0, 0, 6) == UNSUPPORTED  # not a multiple of the 4 consumer warps
     assert L.gqa_set_schedule(0, 0, 0) == OK  # production depths again
+
+
+def test_sources_compile_for_sm100a():
+    """The same sources build for B200's sm_100a (compile check only: the
+    library is tuned for and run on sm_103a; no sm_100a GPU here)."""
+    report = build_lib.build_other_arch("sm_100a")
+    for kernel in ("ctx_nvfp4_kernel", "decode_split_kernel", "decode_merge_kernel", "ctx_merge_kernel"):
+        assert kernel in report and "for 'sm_100a'" in report, kernel
+    assert os.path.exists(os.path.join(ROOT, "gqa_attention_kv_split_gb300", "libgqa_sm100a.so"))
