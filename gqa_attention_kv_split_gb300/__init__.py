@@ -1,10 +1,13 @@
 """Python binding of libgqa -- GB300 (sm_103a) grouped-query attention kernels.
 
 Thin ctypes marshalling over the C ABI declared in ``include/gqa.h``; the
-functions carry the C entry points' names.  PyTorch is used only for device
-memory and the current stream: every step of the computation runs in the
-library's CUDA kernels.  There is no fallback: if ``libgqa.so`` is missing or
-fails to load, every call raises.
+functions carry the C entry points' names.  Tensors are passed as gqa_tensor
+descriptors (data pointer, dtype, device, shape, strides) to the *_t entry
+points, which check dtype, shape, strides and placement in C; a rejected
+call raises GqaError with the library's message.  PyTorch is used only for
+device memory and the current stream: every step of the computation runs in
+the library's CUDA kernels.  There is no fallback: if ``libgqa.so`` is
+missing or fails to load, every call raises.
 
     gqa_decode(q, kv, seq_lens, *, out=None, q_scale=1.0)
     nvfp4_paged_ctx_attn(q_fp8, k_fp4, k_sf, v_fp4, v_sf, block_table, qo_indptr, kv_lens,
@@ -31,6 +34,32 @@ HQ, HKV, D, PAGE = 32, 8, 128, 64
 
 _STATUS = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_UNSUPPORTED", 3: "GQA_ERR_DEVICE_MISMATCH",
            4: "GQA_ERR_CUDA", 5: "GQA_ERR_OOM", 6: "GQA_ERR_TIMEOUT"}
+
+
+class GqaTensor(ctypes.Structure):
+    """gqa_tensor of include/gqa.h."""
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("device", ctypes.c_int32),
+                ("ndim", ctypes.c_int32), ("shape", ctypes.c_int64 * 6), ("strides", ctypes.c_int64 * 6)]
+
+
+_DTYPES = {torch.float16: 1, torch.float8_e4m3fn: 2, torch.uint8: 3, torch.int32: 4, torch.float32: 5}
+
+
+def _desc(t: torch.Tensor, name: str) -> GqaTensor:
+    """Descriptor of a tensor (the library checks it)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dim() > 6:
+        raise ValueError(f"{name} has more than 6 dimensions")
+    d = GqaTensor()
+    d.data = t.data_ptr()
+    d.dtype = _DTYPES.get(t.dtype, 0)
+    d.device = t.device.index if t.is_cuda else -1
+    d.ndim = t.dim()
+    for i, (n, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = n
+        d.strides[i] = st
+    return d
 
 
 class GqaError(RuntimeError):
@@ -62,6 +91,13 @@ def lib() -> ctypes.CDLL:
             vp, i32p, i64, f32 = c.c_void_p, c.c_void_p, c.c_int64, c.c_float
             L.gqa_last_error.restype = c.c_char_p
             L.gqa_version.restype = c.c_int
+            tp = c.POINTER(GqaTensor)
+            L.gqa_decode_t.argtypes = [tp, tp, tp, tp, f32, vp]
+            L.gqa_decode_t.restype = c.c_int
+            L.gqa_decode_paged_t.argtypes = [tp, tp, tp, tp, tp, tp, f32, vp]
+            L.gqa_decode_paged_t.restype = c.c_int
+            L.nvfp4_paged_ctx_attn_t.argtypes = [tp, f32, tp, tp, tp, tp, tp, tp, tp, tp, f32, vp]
+            L.nvfp4_paged_ctx_attn_t.restype = c.c_int
             L.gqa_decode.argtypes = [vp, vp, i32p, vp, i64, i64, f32, vp]
             L.gqa_decode.restype = c.c_int
             L.nvfp4_paged_ctx_attn.argtypes = [vp, f32, vp, vp, vp, vp, i32p, i32p, i32p, vp, f32,
@@ -125,6 +161,10 @@ def _p(t: torch.Tensor):
 _E4M3 = (torch.uint8, torch.float8_e4m3fn)
 
 
+def _ref(d):
+    return ctypes.byref(d)
+
+
 def gqa_decode(q: torch.Tensor, kv: torch.Tensor, seq_lens: torch.Tensor, *, out: torch.Tensor | None = None,
                q_scale: float = 1.0) -> torch.Tensor:
     """FP16 GQA decode of one token per sequence (see include/gqa.h).
@@ -133,16 +173,10 @@ def gqa_decode(q: torch.Tensor, kv: torch.Tensor, seq_lens: torch.Tensor, *, out
     CUDA device (asynchronous on its current stream) or all on the host
     (staged through the device, synchronous).
     """
-    B = q.shape[0]
-    _need(q, "q", (torch.float16,), (B, HQ, D))
-    if kv.dim() != 5:
-        raise ValueError("kv must be [batch, 2, 8, capacity, 128]")
-    _need(kv, "kv", (torch.float16,), (B, 2, HKV, kv.shape[3], D))
-    _need(seq_lens, "sequence_lengths", (torch.int32,), (B,))
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", (torch.float16,), (B, HQ, D))
-    _check(lib().gqa_decode(_p(q), _p(kv), _p(seq_lens), _p(out), B, kv.shape[3], float(q_scale), _stream_for(q)))
+    ds = [_desc(q, "q"), _desc(kv, "kv"), _desc(seq_lens, "seq_lens"), _desc(out, "out")]
+    _check(lib().gqa_decode_t(*map(_ref, ds), float(q_scale), _stream_for(q)))
     return out
 
 
@@ -152,22 +186,11 @@ def gqa_decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tens
     f16, k_pages / v_pages [num_pages,8,64,128] f16, block_table
     [B, max_pages_per_seq] int32, seq_lens [B] int32, all on one CUDA device
     or all on the host."""
-    B = q.shape[0]
-    _need(q, "q", (torch.float16,), (B, HQ, D))
-    if k_pages.dim() != 4:
-        raise ValueError("k_pages must be [num_pages, 8, 64, 128]")
-    P = k_pages.shape[0]
-    _need(k_pages, "k_pages", (torch.float16,), (P, HKV, 64, D))
-    _need(v_pages, "v_pages", (torch.float16,), (P, HKV, 64, D))
-    if block_table.dim() != 2:
-        raise ValueError("block_table must be [batch, max_pages_per_seq]")
-    _need(block_table, "block_table", (torch.int32,), (B, block_table.shape[1]))
-    _need(seq_lens, "sequence_lengths", (torch.int32,), (B,))
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", (torch.float16,), (B, HQ, D))
-    _check(lib().gqa_decode_paged(_p(q), _p(k_pages), _p(v_pages), _p(block_table), _p(seq_lens), _p(out), B, P,
-                                  block_table.shape[1], float(q_scale), _stream_for(q)))
+    ds = [_desc(q, "q"), _desc(k_pages, "k_pages"), _desc(v_pages, "v_pages"), _desc(block_table, "block_table"),
+          _desc(seq_lens, "seq_lens"), _desc(out, "out")]
+    _check(lib().gqa_decode_paged_t(*map(_ref, ds), float(q_scale), _stream_for(q)))
     return out
 
 
@@ -194,25 +217,13 @@ def nvfp4_paged_ctx_attn(q_fp8, k_fp4, k_sf, v_fp4, v_sf, block_table, qo_indptr
 
     Returns out_fp8 [total_q,32,128] as uint8 E4M3 codes (or writes `out`).
     """
-    T = q_fp8.shape[0]
-    _need(q_fp8, "q_fp8", _E4M3, (T, HQ, D))
-    P = k_fp4.shape[0]
-    _need(k_fp4, "k_fp4", (torch.uint8,), (P, HKV, PAGE, D // 2))
-    _need(v_fp4, "v_fp4", (torch.uint8,), (P, HKV, PAGE, D // 2))
-    _need(k_sf, "k_sf", _E4M3, (P, HKV, PAGE, D // 16))
-    _need(v_sf, "v_sf", _E4M3, (P, HKV, PAGE, D // 16))
-    B = kv_lens.shape[0]
-    _need(block_table, "block_table", (torch.int32,))
-    if block_table.dim() != 2 or block_table.shape[0] != B:
-        raise ValueError("block_table must be [batch, max_pages_per_seq]")
-    _need(qo_indptr, "qo_indptr", (torch.int32,), (B + 1,))
-    _need(kv_lens, "kv_lens", (torch.int32,), (B,))
     if out is None:
-        out = torch.empty((T, HQ, D), dtype=torch.uint8, device=q_fp8.device)
-    _need(out, "out", _E4M3, (T, HQ, D))
-    _check(lib().nvfp4_paged_ctx_attn(
-        _p(q_fp8), float(q_scale), _p(k_fp4), _p(k_sf), _p(v_fp4), _p(v_sf), _p(block_table), _p(qo_indptr),
-        _p(kv_lens), _p(out), float(out_scale), B, T, P, block_table.shape[1], _stream_for(q_fp8)))
+        out = torch.empty((q_fp8.shape[0], HQ, D), dtype=torch.uint8, device=q_fp8.device)
+    ds = [_desc(t, n) for t, n in ((q_fp8, "q_fp8"), (k_fp4, "k_fp4"), (k_sf, "k_sf"), (v_fp4, "v_fp4"),
+                                   (v_sf, "v_sf"), (block_table, "block_table"), (qo_indptr, "qo_indptr"),
+                                   (kv_lens, "kv_lens"), (out, "out_fp8"))]
+    r = list(map(_ref, ds))
+    _check(lib().nvfp4_paged_ctx_attn_t(r[0], float(q_scale), *r[1:9], float(out_scale), _stream_for(q_fp8)))
     return out
 
 

@@ -14,6 +14,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
+#include <initializer_list>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -98,8 +99,12 @@ struct Arg {
   size_t align;
 };
 
-// All pointers on one side: either the same device or all host.
-gqa_status locate(const std::vector<Arg>& args, Where* out) {
+constexpr int kAnyDevice = -1000;  // no expectation from a descriptor
+
+// All pointers on one side: either the same device or all host; when
+// `expect` is a descriptor's device field (-1 = host), the memory must be
+// there.
+gqa_status locate(const std::vector<Arg>& args, Where* out, int expect = kAnyDevice) {
   for (const Arg& a : args)
     if (a.p == nullptr) return fail(GQA_ERR_INVALID_ARG, "%s is a null pointer", a.name);
   Where first{};
@@ -117,6 +122,10 @@ gqa_status locate(const std::vector<Arg>& args, Where* out) {
     if (!w.host && (reinterpret_cast<uintptr_t>(args[i].p) % args[i].align) != 0)
       return fail(GQA_ERR_INVALID_ARG, "%s is not %zu-byte aligned", args[i].name, args[i].align);
   }
+  const int real = first.host ? -1 : first.device;
+  if (expect != kAnyDevice && real != expect)
+    return fail(GQA_ERR_DEVICE_MISMATCH, "the descriptors say device %d but the memory is on %s %d", expect,
+                first.host ? "host" : "device", first.device);
   *out = first;
   return GQA_OK;
 }
@@ -172,6 +181,73 @@ struct Carver {
   }
 };
 
+// ---- tensor descriptors (gqa_tensor) ---------------------------------------
+
+const char* dtype_name(int32_t d) {
+  switch (d) {
+    case GQA_F16: return "f16";
+    case GQA_E4M3: return "e4m3";
+    case GQA_U8: return "u8";
+    case GQA_I32: return "i32";
+    case GQA_F32: return "f32";
+    default: return "unknown";
+  }
+}
+
+// Structural check of one descriptor: non-null, an accepted dtype, the rank
+// and shape asked for (-1 = any extent, returned in got[]), dense row-major
+// strides (in elements; a dimension of extent 1 may carry any stride).  No
+// CUDA call: it runs before anything touches the device.
+gqa_status check_desc(const gqa_tensor* t, const char* name, std::initializer_list<int32_t> dtypes,
+                      std::initializer_list<int64_t> shape, int64_t* got = nullptr) {
+  if (!t) return fail(GQA_ERR_INVALID_ARG, "%s: null descriptor", name);
+  if (!t->data) return fail(GQA_ERR_INVALID_ARG, "%s is a null pointer", name);
+  bool dt_ok = false;
+  for (int32_t d : dtypes) dt_ok |= (t->dtype == d);
+  if (!dt_ok) {
+    std::string want;
+    for (int32_t d : dtypes) want += std::string(want.empty() ? "" : " or ") + dtype_name(d);
+    return fail(GQA_ERR_INVALID_ARG, "%s has dtype %s; expected %s", name, dtype_name(t->dtype), want.c_str());
+  }
+  const int nd = (int)shape.size();
+  if (t->ndim != nd) return fail(GQA_ERR_INVALID_ARG, "%s has %d dimensions; expected %d", name, t->ndim, nd);
+  int i = 0;
+  for (int64_t want : shape) {
+    const int64_t have = t->shape[i];
+    if (have < 0) return fail(GQA_ERR_INVALID_ARG, "%s: negative extent in dimension %d", name, i);
+    if (want >= 0 && have != want)
+      return fail(GQA_ERR_UNSUPPORTED_SHAPE, "%s has extent %lld in dimension %d; expected %lld", name,
+                  (long long)have, i, (long long)want);
+    if (got) got[i] = have;
+    ++i;
+  }
+  int64_t expect = 1;
+  for (int d = nd - 1; d >= 0; --d) {
+    if (t->shape[d] != 1 && t->strides[d] != expect)
+      return fail(GQA_ERR_INVALID_ARG, "%s is not dense row-major (stride %lld in dimension %d; expected %lld)", name,
+                  (long long)t->strides[d], d, (long long)expect);
+    expect *= t->shape[d];
+  }
+  return GQA_OK;
+}
+
+// Every descriptor names the same device (or all host memory, device -1).
+// (Where the memory really is, is checked once per pointer by locate().)
+gqa_status check_devices(std::initializer_list<std::pair<const gqa_tensor*, const char*>> ts) {
+  const gqa_tensor* first = ts.begin()->first;
+  for (const auto& t : ts)
+    if (t.first->device != first->device)
+      return fail(GQA_ERR_DEVICE_MISMATCH, "%s is on device %d but %s is on device %d", t.second, t.first->device,
+                  ts.begin()->second, first->device);
+  return GQA_OK;
+}
+
+#define GQA_TRY(expr)                  \
+  do {                                 \
+    gqa_status _s = (expr);            \
+    if (_s != GQA_OK) return _s;       \
+  } while (0)
+
 std::atomic<int> g_starve{0};
 std::atomic<int> g_ctx_stages{0}, g_ctx_slots{0}, g_decode_stages{0};
 
@@ -190,15 +266,17 @@ const char* gqa_last_error(void) { return t_last_error.c_str(); }
 
 int gqa_version(void) { return 300; }  // 0.3.0: qo_indptr checked on the device, gqa_debug_starve_producers
 
-gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
-                      int64_t capacity, float q_scale, gqa_stream_t stream_) {
+namespace {
+gqa_status decode_impl(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
+                       int64_t capacity, float q_scale, gqa_stream_t stream_, int expect) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (batch < 1 || batch > 65535) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 65535]", (long long)batch);
   if (capacity < 1 || capacity > 2147483647LL)
     return fail(GQA_ERR_UNSUPPORTED, "capacity %lld outside [1, 2^31-1]", (long long)capacity);
   if (!std::isfinite(q_scale)) return fail(GQA_ERR_INVALID_ARG, "q_scale is not finite");
   Where where;
-  gqa_status st = locate({{q, "q", 16}, {kv, "kv", 16}, {seq_lens, "seq_lens", 4}, {out, "out", 16}}, &where);
+  gqa_status st =
+      locate({{q, "q", 16}, {kv, "kv", 16}, {seq_lens, "seq_lens", 4}, {out, "out", 16}}, &where, expect);
   if (st != GQA_OK) return st;
 
   const gqa::DecodePlan plan = gqa::plan_decode(batch, capacity);
@@ -249,9 +327,9 @@ gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, vo
   return GQA_OK;
 }
 
-gqa_status gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
-                            const int32_t* seq_lens, void* out, int64_t batch, int64_t num_pages,
-                            int64_t max_pages_per_seq, float q_scale, gqa_stream_t stream_) {
+gqa_status decode_paged_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                             const int32_t* seq_lens, void* out, int64_t batch, int64_t num_pages,
+                             int64_t max_pages_per_seq, float q_scale, gqa_stream_t stream_, int expect) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (batch < 1 || batch > 65535) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 65535]", (long long)batch);
   if (num_pages < 1 || num_pages > 2147483647LL)
@@ -266,7 +344,7 @@ gqa_status gqa_decode_paged(const void* q, const void* k_pages, const void* v_pa
                           {block_table, "block_table", 4},
                           {seq_lens, "seq_lens", 4},
                           {out, "out", 16}},
-                         &where);
+                         &where, expect);
   if (st != GQA_OK) return st;
   const int64_t capacity = max_pages_per_seq * 64;
   const gqa::DecodePlan plan = gqa::plan_decode(batch, capacity);
@@ -328,6 +406,19 @@ gqa_status gqa_decode_paged(const void* q, const void* k_pages, const void* v_pa
   GQA_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
   return GQA_OK;
 }
+}  // namespace
+
+gqa_status gqa_decode(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
+                      int64_t capacity, float q_scale, gqa_stream_t stream) {
+  return decode_impl(q, kv, seq_lens, out, batch, capacity, q_scale, stream, kAnyDevice);
+}
+
+gqa_status gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
+                            const int32_t* seq_lens, void* out, int64_t batch, int64_t num_pages,
+                            int64_t max_pages_per_seq, float q_scale, gqa_stream_t stream) {
+  return decode_paged_impl(q, k_pages, v_pages, block_table, seq_lens, out, batch, num_pages, max_pages_per_seq,
+                           q_scale, stream, kAnyDevice);
+}
 
 gqa_status gqa_decode_noalloc(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
                               int64_t capacity, float q_scale, gqa_stream_t stream_) {
@@ -381,11 +472,11 @@ gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_se
   return GQA_OK;
 }
 
-gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_fp4, const void* k_sf,
-                                const void* v_fp4, const void* v_sf, const int32_t* block_table,
-                                const int32_t* qo_indptr, const int32_t* kv_lens, void* out_fp8,
-                                float out_scale, int64_t batch, int64_t total_q, int64_t num_pages,
-                                int64_t max_pages_per_seq, gqa_stream_t stream_) {
+namespace {
+gqa_status ctx_impl(const void* q_fp8, float q_scale, const void* k_fp4, const void* k_sf, const void* v_fp4,
+                    const void* v_sf, const int32_t* block_table, const int32_t* qo_indptr, const int32_t* kv_lens,
+                    void* out_fp8, float out_scale, int64_t batch, int64_t total_q, int64_t num_pages,
+                    int64_t max_pages_per_seq, gqa_stream_t stream_, int expect) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (batch < 1 || batch > (1 << 20))
     return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 2^20]", (long long)batch);
@@ -405,7 +496,7 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
                           {qo_indptr, "qo_indptr", 4},
                           {kv_lens, "kv_lens", 4},
                           {out_fp8, "out_fp8", 16}},
-                         &where);
+                         &where, expect);
   if (st != GQA_OK) return st;
 
   gqa::CtxArgs a;
@@ -492,6 +583,16 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
   GQA_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
   return GQA_OK;
 }
+}  // namespace
+
+gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_fp4, const void* k_sf,
+                                const void* v_fp4, const void* v_sf, const int32_t* block_table,
+                                const int32_t* qo_indptr, const int32_t* kv_lens, void* out_fp8, float out_scale,
+                                int64_t batch, int64_t total_q, int64_t num_pages, int64_t max_pages_per_seq,
+                                gqa_stream_t stream) {
+  return ctx_impl(q_fp8, q_scale, k_fp4, k_sf, v_fp4, v_sf, block_table, qo_indptr, kv_lens, out_fp8, out_scale,
+                  batch, total_q, num_pages, max_pages_per_seq, stream, kAnyDevice);
+}
 
 gqa_status gqa_debug_dequant_pages(const void* fp4, const void* sf, const int32_t* block_table,
                                    const int32_t* kv_lens, void* out_e4m3, int64_t batch, int64_t num_pages,
@@ -557,6 +658,61 @@ gqa_status gqa_check_device_errors(int device, uint32_t* word) {
                 "non-decreasing from 0 to total_q, bit 3 = dequantisation self-check (error word 0x%x)",
                 *word);
   return GQA_OK;
+}
+
+// ---- descriptor forms of the three operations --------------------------------
+
+gqa_status gqa_decode_t(const gqa_tensor* q, const gqa_tensor* kv, const gqa_tensor* seq_lens, gqa_tensor* out,
+                        float q_scale, gqa_stream_t stream) {
+  int64_t qs[3], ks[5];
+  GQA_TRY(check_desc(q, "q", {GQA_F16}, {-1, 32, 128}, qs));
+  GQA_TRY(check_desc(kv, "kv", {GQA_F16}, {qs[0], 2, 8, -1, 128}, ks));
+  GQA_TRY(check_desc(seq_lens, "seq_lens", {GQA_I32}, {qs[0]}));
+  GQA_TRY(check_desc(out, "out", {GQA_F16}, {qs[0], 32, 128}));
+  GQA_TRY(check_devices({{q, "q"}, {kv, "kv"}, {seq_lens, "seq_lens"}, {out, "out"}}));
+  return decode_impl(q->data, kv->data, static_cast<const int32_t*>(seq_lens->data), out->data, qs[0], ks[3], q_scale,
+                     stream, q->device);
+}
+
+gqa_status gqa_decode_paged_t(const gqa_tensor* q, const gqa_tensor* k_pages, const gqa_tensor* v_pages,
+                              const gqa_tensor* block_table, const gqa_tensor* seq_lens, gqa_tensor* out,
+                              float q_scale, gqa_stream_t stream) {
+  int64_t qs[3], ps[4], bs[2];
+  GQA_TRY(check_desc(q, "q", {GQA_F16}, {-1, 32, 128}, qs));
+  GQA_TRY(check_desc(k_pages, "k_pages", {GQA_F16}, {-1, 8, 64, 128}, ps));
+  GQA_TRY(check_desc(v_pages, "v_pages", {GQA_F16}, {ps[0], 8, 64, 128}));
+  GQA_TRY(check_desc(block_table, "block_table", {GQA_I32}, {qs[0], -1}, bs));
+  GQA_TRY(check_desc(seq_lens, "seq_lens", {GQA_I32}, {qs[0]}));
+  GQA_TRY(check_desc(out, "out", {GQA_F16}, {qs[0], 32, 128}));
+  GQA_TRY(check_devices({{q, "q"}, {k_pages, "k_pages"}, {v_pages, "v_pages"}, {block_table, "block_table"},
+                         {seq_lens, "seq_lens"}, {out, "out"}}));
+  return decode_paged_impl(q->data, k_pages->data, v_pages->data, static_cast<const int32_t*>(block_table->data),
+                           static_cast<const int32_t*>(seq_lens->data), out->data, qs[0], ps[0], bs[1], q_scale, stream,
+                           q->device);
+}
+
+gqa_status nvfp4_paged_ctx_attn_t(const gqa_tensor* q_fp8, float q_scale, const gqa_tensor* k_fp4,
+                                  const gqa_tensor* k_sf, const gqa_tensor* v_fp4, const gqa_tensor* v_sf,
+                                  const gqa_tensor* block_table, const gqa_tensor* qo_indptr,
+                                  const gqa_tensor* kv_lens, gqa_tensor* out_fp8, float out_scale,
+                                  gqa_stream_t stream) {
+  int64_t qs[3], ps[4], ls[1], bs[2];
+  GQA_TRY(check_desc(q_fp8, "q_fp8", {GQA_E4M3, GQA_U8}, {-1, 32, 128}, qs));
+  GQA_TRY(check_desc(k_fp4, "k_fp4", {GQA_U8}, {-1, 8, 64, 64}, ps));
+  GQA_TRY(check_desc(k_sf, "k_sf", {GQA_E4M3, GQA_U8}, {ps[0], 8, 64, 8}));
+  GQA_TRY(check_desc(v_fp4, "v_fp4", {GQA_U8}, {ps[0], 8, 64, 64}));
+  GQA_TRY(check_desc(v_sf, "v_sf", {GQA_E4M3, GQA_U8}, {ps[0], 8, 64, 8}));
+  GQA_TRY(check_desc(kv_lens, "kv_lens", {GQA_I32}, {-1}, ls));
+  GQA_TRY(check_desc(qo_indptr, "qo_indptr", {GQA_I32}, {ls[0] + 1}));
+  GQA_TRY(check_desc(block_table, "block_table", {GQA_I32}, {ls[0], -1}, bs));
+  GQA_TRY(check_desc(out_fp8, "out_fp8", {GQA_E4M3, GQA_U8}, {qs[0], 32, 128}));
+  GQA_TRY(check_devices({{q_fp8, "q_fp8"}, {k_fp4, "k_fp4"}, {k_sf, "k_sf"}, {v_fp4, "v_fp4"}, {v_sf, "v_sf"},
+                         {block_table, "block_table"}, {qo_indptr, "qo_indptr"}, {kv_lens, "kv_lens"},
+                         {out_fp8, "out_fp8"}}));
+  return ctx_impl(q_fp8->data, q_scale, k_fp4->data, k_sf->data, v_fp4->data, v_sf->data,
+                  static_cast<const int32_t*>(block_table->data), static_cast<const int32_t*>(qo_indptr->data),
+                  static_cast<const int32_t*>(kv_lens->data), out_fp8->data, out_scale, ls[0], qs[0], ps[0], bs[1],
+                  stream, q_fp8->device);
 }
 
 gqa_status gqa_release_workspace(void) {

@@ -51,13 +51,45 @@ typedef struct CUstream_st* gqa_stream_t;
 
 typedef enum gqa_status {
   GQA_OK = 0,
-  GQA_ERR_INVALID_ARG = 1,      /* null pointer, bad size, misalignment */
-  GQA_ERR_UNSUPPORTED = 2,      /* shape outside what the kernels handle */
-  GQA_ERR_DEVICE_MISMATCH = 3,  /* pointers on different devices / host+device mix */
-  GQA_ERR_CUDA = 4,             /* a CUDA runtime call failed */
-  GQA_ERR_OOM = 5,              /* workspace allocation failed */
-  GQA_ERR_TIMEOUT = 6           /* a kernel's bounded wait expired (see gqa_check_device_errors) */
+  GQA_ERR_INVALID_ARG = 1,        /* null pointer, bad size, dtype or strides, misalignment */
+  GQA_ERR_UNSUPPORTED = 2,        /* shape outside what the kernels handle */
+  GQA_ERR_UNSUPPORTED_SHAPE = 2,  /* (the same code, by the name the descriptor entry points use) */
+  GQA_ERR_DEVICE_MISMATCH = 3,    /* pointers on different devices / host+device mix */
+  GQA_ERR_CUDA = 4,               /* a CUDA runtime call failed */
+  GQA_ERR_OOM = 5,                /* workspace allocation failed */
+  GQA_ERR_TIMEOUT = 6             /* a kernel's bounded wait expired (see gqa_check_device_errors) */
 } gqa_status;
+
+/*
+ * Tensor descriptor of the *_t entry points below: the pointer entry points'
+ * arguments plus what a C caller would otherwise have to get right unaided --
+ * element type, placement, shape and strides -- so that the library can
+ * check them (a DLPack-like record of our own).
+ *
+ *   data     first element (device or host memory)
+ *   dtype    a gqa_dtype
+ *   device   CUDA device ordinal of `data`, or -1 for host memory; checked
+ *            against where the memory really is
+ *   ndim     number of dimensions (<= 6)
+ *   shape    extents; strides in elements, dense row-major required (a
+ *            dimension of extent 1 may carry any stride)
+ */
+typedef enum gqa_dtype {
+  GQA_F16 = 1,   /* IEEE binary16 */
+  GQA_E4M3 = 2,  /* OCP FP8 E4M3 ("fn") bytes */
+  GQA_U8 = 3,    /* bytes: packed E2M1 pairs, or E4M3 codes given as raw bytes */
+  GQA_I32 = 4,
+  GQA_F32 = 5
+} gqa_dtype;
+
+typedef struct gqa_tensor {
+  void* data;
+  int32_t dtype;
+  int32_t device;
+  int32_t ndim;
+  int64_t shape[6];
+  int64_t strides[6];
+} gqa_tensor;
 
 /* Message for the last non-OK status returned on this thread. */
 const char* gqa_last_error(void);
@@ -154,6 +186,31 @@ gqa_status gqa_decode_noalloc(const void* q, const void* kv, const int32_t* seq_
 gqa_status gqa_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int32_t* block_table,
                             const int32_t* seq_lens, void* out, int64_t batch, int64_t num_pages,
                             int64_t max_pages_per_seq, float q_scale, gqa_stream_t stream);
+
+/*
+ * Descriptor forms of gqa_decode, gqa_decode_paged and nvfp4_paged_ctx_attn:
+ * the same operations, with every tensor given as a gqa_tensor.  Before any
+ * CUDA work they check each descriptor's dtype, rank, shape (including the
+ * extents the tensors share: batch, pages, total_q), dense row-major strides
+ * and non-null data -- GQA_ERR_INVALID_ARG, or GQA_ERR_UNSUPPORTED_SHAPE for
+ * an extent the kernels do not handle (32 query heads, 8 KV heads, head dim
+ * 128, 64-token pages) -- then that all tensors share one `device` field and
+ * that the memory really is there (GQA_ERR_DEVICE_MISMATCH); then they call
+ * the pointer form with the sizes read from the shapes.  Accepted dtypes:
+ * q/kv/out/pages of the decodes GQA_F16; q_fp8, k_sf, v_sf, out_fp8 GQA_E4M3
+ * or GQA_U8; k_fp4, v_fp4 GQA_U8; seq_lens, block_table, qo_indptr, kv_lens
+ * GQA_I32.  Shapes as in the pointer forms' comments.
+ */
+gqa_status gqa_decode_t(const gqa_tensor* q, const gqa_tensor* kv, const gqa_tensor* seq_lens, gqa_tensor* out,
+                        float q_scale, gqa_stream_t stream);
+gqa_status gqa_decode_paged_t(const gqa_tensor* q, const gqa_tensor* k_pages, const gqa_tensor* v_pages,
+                              const gqa_tensor* block_table, const gqa_tensor* seq_lens, gqa_tensor* out,
+                              float q_scale, gqa_stream_t stream);
+gqa_status nvfp4_paged_ctx_attn_t(const gqa_tensor* q_fp8, float q_scale, const gqa_tensor* k_fp4,
+                                  const gqa_tensor* k_sf, const gqa_tensor* v_fp4, const gqa_tensor* v_sf,
+                                  const gqa_tensor* block_table, const gqa_tensor* qo_indptr,
+                                  const gqa_tensor* kv_lens, gqa_tensor* out_fp8, float out_scale,
+                                  gqa_stream_t stream);
 
 /*
  * gqa_decode_plan -- how gqa_decode splits the KV sequence for a given batch

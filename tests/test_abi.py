@@ -116,34 +116,92 @@ def test_python_binding_raises_without_library(monkeypatch):
                        torch.ones(1, dtype=torch.int32))
 
 
-def test_python_binding_checks_shapes_and_dtypes():
+def test_descriptor_checks_shapes_dtypes_and_strides():
+    """The *_t entry points check every descriptor in C before any CUDA call
+    (so this runs without a GPU); the binding only marshals."""
     import torch
-    with pytest.raises(TypeError):
+    with pytest.raises(gqa.GqaError, match="q has dtype f32; expected f16"):
         gqa.gqa_decode(torch.zeros(1, 32, 128), torch.zeros(1, 2, 8, 4, 128, dtype=torch.float16),
                        torch.ones(1, dtype=torch.int32))
-    with pytest.raises(ValueError):
+    with pytest.raises(gqa.GqaError, match="UNSUPPORTED.*kv has extent 4 in dimension 2; expected 8"):
         gqa.gqa_decode(torch.zeros(1, 32, 128, dtype=torch.float16),
                        torch.zeros(1, 2, 4, 4, 128, dtype=torch.float16), torch.ones(1, dtype=torch.int32))
+    with pytest.raises(gqa.GqaError, match="seq_lens has extent 2 in dimension 0; expected 1"):
+        gqa.gqa_decode(torch.zeros(1, 32, 128, dtype=torch.float16),
+                       torch.zeros(1, 2, 8, 4, 128, dtype=torch.float16), torch.ones(2, dtype=torch.int32))
+    with pytest.raises(gqa.GqaError, match="kv is not dense row-major"):
+        gqa.gqa_decode(torch.zeros(1, 32, 128, dtype=torch.float16),
+                       torch.zeros(1, 2, 8, 8, 128, dtype=torch.float16)[:, :, :, ::2], torch.ones(1, dtype=torch.int32))
 
 
-def test_python_binding_checks_paged_decode_arguments():
+def test_descriptor_checks_paged_decode_arguments():
     import torch
     q = torch.zeros(1, 32, 128, dtype=torch.float16)
     pages = torch.zeros(3, 8, 64, 128, dtype=torch.float16)
     bt = torch.zeros(1, 2, dtype=torch.int32)
     lens = torch.ones(1, dtype=torch.int32)
-    with pytest.raises(TypeError):   # pages must be fp16
+    with pytest.raises(gqa.GqaError, match="k_pages has dtype f32"):   # pages must be fp16
         gqa.gqa_decode_paged(q, pages.float(), pages, bt, lens)
-    with pytest.raises(ValueError):  # 64-token pages of 8 heads
+    with pytest.raises(gqa.GqaError, match="UNSUPPORTED"):  # 64-token pages of 8 heads
         gqa.gqa_decode_paged(q, torch.zeros(3, 8, 32, 128, dtype=torch.float16), pages, bt, lens)
-    with pytest.raises(ValueError):  # K and V pages alike
+    with pytest.raises(gqa.GqaError, match="v_pages has extent 2"):  # K and V pages alike
         gqa.gqa_decode_paged(q, pages, torch.zeros(2, 8, 64, 128, dtype=torch.float16), bt, lens)
-    with pytest.raises(ValueError):  # one table row per sequence
+    with pytest.raises(gqa.GqaError, match="block_table has extent 2 in dimension 0"):  # one row per sequence
         gqa.gqa_decode_paged(q, pages, pages, torch.zeros(2, 2, dtype=torch.int32), lens)
-    with pytest.raises(TypeError):   # int32 table
+    with pytest.raises(gqa.GqaError, match="block_table has dtype unknown"):   # int32 table
         gqa.gqa_decode_paged(q, pages, pages, bt.long(), lens)
-    with pytest.raises(ValueError):  # contiguous
+    with pytest.raises(gqa.GqaError, match="not dense row-major"):  # contiguous
         gqa.gqa_decode_paged(q, pages, pages, torch.zeros(1, 4, dtype=torch.int32)[:, ::2], lens)
+
+
+def test_descriptor_checks_context_arguments():
+    import torch
+    T, P, B = 5, 3, 2
+    q = torch.zeros(T, 32, 128, dtype=torch.uint8)
+    fp4 = torch.zeros(P, 8, 64, 64, dtype=torch.uint8)
+    sf = torch.zeros(P, 8, 64, 8, dtype=torch.uint8)
+    bt = torch.zeros(B, 2, dtype=torch.int32)
+    qi = torch.tensor([0, 2, 5], dtype=torch.int32)
+    kl = torch.tensor([3, 3], dtype=torch.int32)
+    call = lambda **kw: gqa.nvfp4_paged_ctx_attn(*[kw.get(n, v) for n, v in (
+        ("q", q), ("kf", fp4), ("ks", sf), ("vf", fp4), ("vs", sf), ("bt", bt), ("qi", qi), ("kl", kl))])
+    with pytest.raises(gqa.GqaError, match="UNSUPPORTED.*q_fp8 has extent 16 in dimension 1"):
+        call(q=torch.zeros(T, 16, 128, dtype=torch.uint8))
+    with pytest.raises(gqa.GqaError, match="k_fp4 has dtype f16"):
+        call(kf=fp4.half())
+    with pytest.raises(gqa.GqaError, match="v_sf has extent 2 in dimension 0; expected 3"):
+        call(vs=torch.zeros(2, 8, 64, 8, dtype=torch.uint8))
+    with pytest.raises(gqa.GqaError, match="qo_indptr has extent 2 in dimension 0; expected 3"):
+        call(qi=torch.tensor([0, 5], dtype=torch.int32))
+    with pytest.raises(gqa.GqaError, match="block_table has extent 3 in dimension 0"):
+        call(bt=torch.zeros(3, 2, dtype=torch.int32))
+    with pytest.raises(gqa.GqaError, match="out_fp8 has extent 4 in dimension 0"):
+        gqa.nvfp4_paged_ctx_attn(q, fp4, sf, fp4, sf, bt, qi, kl, out=torch.zeros(4, 32, 128, dtype=torch.uint8))
+
+
+def test_descriptor_checks_in_c(L):
+    """The same checks reached from C with hand-made descriptors: a null
+    descriptor, a null data pointer, more dimensions than declared, and
+    device fields that disagree -- all before any CUDA call."""
+    import torch
+    q = torch.zeros(1, 32, 128, dtype=torch.float16)
+    kv = torch.zeros(1, 2, 8, 4, 128, dtype=torch.float16)
+    lens = torch.ones(1, dtype=torch.int32)
+    d = [gqa._desc(t, n) for t, n in ((q, "q"), (kv, "kv"), (lens, "lens"), (q, "out"))]
+    r = lambda: [ctypes.byref(x) for x in d]
+    assert L.gqa_decode_t(None, *r()[1:], 1.0, P(0)) == INVALID
+    assert b"null descriptor" in L.gqa_last_error()
+    d[0].data = None
+    assert L.gqa_decode_t(*r(), 1.0, P(0)) == INVALID
+    assert b"q is a null pointer" in L.gqa_last_error()
+    d[0].data = q.data_ptr()
+    d[2].ndim = 2
+    assert L.gqa_decode_t(*r(), 1.0, P(0)) == INVALID
+    assert b"seq_lens has 2 dimensions; expected 1" in L.gqa_last_error()
+    d[2].ndim = 1
+    d[3].device = 0  # out claims device 0, the others host
+    assert L.gqa_decode_t(*r(), 1.0, P(0)) == 3  # GQA_ERR_DEVICE_MISMATCH
+    assert b"out is on device 0" in L.gqa_last_error()
 
 
 def test_decode_plan_covers_capacity():
