@@ -62,6 +62,8 @@ ALL_CONFIGS = ["decode_b2_cap256", "decode_b64_cap8192", "decode_b8_cap131072",
 # packed K/V ring" (GB300, its kernel after the change), read as batch x q_len x kv_len: context for the
 # workloads of the same shape, not a target of this metric.
 PAGE_ROWS_US = {"ctx_b2_q1_kv4096": ("2 x 1 x 4096", 44.5), "ctx_b1_q32_kv32768": ("1 x 32 x 32768", 329.8)}
+# Decode-shaped context workloads, reported against HBM (their page bytes) rather than the tensor peak.
+MEMORY_BOUND_CTX = {"ctx_b64_q1_kv8192", "ctx_b64_q8_kv8192"}
 FALLBACK_HBM = 6800.0
 FALLBACK_BF16 = 1900.0
 FP8_OVER_BF16 = 2.0        # nominal dense ratio (4.5 / 2.25 PFLOP/s)
@@ -327,6 +329,15 @@ class Workload:
                     "kernel": ("decode_split_kernel" + (" + decode_merge_kernel" if self.launches > 1 else "")
                                + " inside the same events")}
         fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
+        if self.name in MEMORY_BOUND_CTX:
+            # decode-shaped: a few query rows per KV head, so the page bytes, not the tensor work, bound it
+            gbs = self.x.page_bytes_read() / (ms * 1e-3) / 1e9
+            return {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_nominal": HBM_NOMINAL_GBS,
+                    "frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4),
+                    "algorithmic": f"{self.x.page_bytes_read()} B = every used page's packed codes and scales, "
+                                   "K and V, once", "tflops": round(a, 2),
+                    "kernel": "ctx_nvfp4_kernel" + (" + ctx_merge_kernel" if self.launches > 1 else "")}
         return {"bound": "tensor", "achieved": round(a, 2), "peak": round(fp8, 1), "unit": "TFLOP/s",
                 "frac": round(a / fp8, 4),
                 "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (nominal dense FP8:bf16)",

@@ -18,6 +18,8 @@ structure of the benchmark workloads this library is measured on:
 * ctx_b2_q4096_kv65536  batch 2, q_len 4096 ending a 65536-token KV, seed 4, out_scale 2^-6
 * ctx_b2_q1_kv4096      batch 2, q_len 1 over 4096 keys,            seed 8, out_scale 2^-4
 * ctx_b1_q32_kv32768    batch 1, q_len 32 over 32768 keys,          seed 9, out_scale 2^-6
+* ctx_b64_q1_kv8192     batch 64, q_len 1 over 8192 keys,           seed 10, out_scale 2^-4
+* ctx_b64_q8_kv8192     batch 64, q_len 8 over 8192 keys,           seed 11, out_scale 2^-4
 
 STUDY_WORKLOADS holds shapes used only to profile the kernels (not benchmark
 configurations).  The benchmark generates its inputs on the GPU (CUDA
@@ -147,6 +149,13 @@ class CtxInputs:
     @property
     def total_q(self) -> int:
         return self.q_fp8.shape[0]
+
+    def page_bytes_read(self) -> int:
+        """Packed K/V codes and scales of every page the sequences' visible keys
+        touch, once: 64 tokens x 8 heads x (64 + 8) B per page, K and V."""
+        kl = self.kv_lens.cpu().tolist()
+        pages = sum((n + PAGE - 1) // PAGE for n in kl)
+        return pages * PAGE * HKV * (D // 2 + D // 16) * 2
 
     def causal_flops(self) -> int:
         """4 * D * (visible query/key pairs) * 32 heads, bottom-right causal."""
@@ -284,6 +293,10 @@ CTX_WORKLOADS = {
     # no output scale; powers of two keep their outputs (|O| ~ 2e-2 and ~ 7e-3) in E4M3's normal range.
     "ctx_b2_q1_kv4096": dict(q_lens=[1, 1], kv_lens=[4096, 4096], seed=8, out_scale=2.0 ** -4),
     "ctx_b1_q32_kv32768": dict(q_lens=[32], kv_lens=[32768], seed=9, out_scale=2.0 ** -6),
+    # decode-shaped NVFP4 calls at a realistic batch (64 sequences of 8192 keys, 1 or 8 new queries each):
+    # 512 units, enough to fill the GPU without splitting the KV range; memory-bound (the page bytes)
+    "ctx_b64_q1_kv8192": dict(q_lens=[1] * 64, kv_lens=[8192] * 64, seed=10, out_scale=2.0 ** -4),
+    "ctx_b64_q8_kv8192": dict(q_lens=[8] * 64, kv_lens=[8192] * 64, seed=11, out_scale=2.0 ** -4),
 }
 
 # Not benchmark configurations: shapes used only to profile or study the kernels.

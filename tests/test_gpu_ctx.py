@@ -237,6 +237,15 @@ def test_workload_b4_q2048_kv2048_full():
     check_ctx(run_dev(xd), ref(xh), "ctx_b4_q2048_kv2048")
 
 
+@pytest.mark.parametrize("name", ["ctx_b64_q1_kv8192", "ctx_b64_q8_kv8192"])
+def test_decode_shaped_workloads_full(name):
+    """Decode-shaped NVFP4 calls at a realistic batch (64 sequences of 8192
+    keys, 1 or 8 queries): every row, the benchmark's device-generated inputs."""
+    xd, xh = device_workload(name)
+    assert plan_of(xh)["num_splits"] == 1  # 512 units fill the GPU
+    check_ctx(run_dev(xd), ref(xh), name)
+
+
 def _b2_q4096_kv65536_items():
     """5120 (row, head) items: all 32 heads of 128 rows -- the first and last
     query rows of both sequences, rows on either side of the 32-query M-tile
