@@ -24,7 +24,7 @@ import torch
 
 __all__ = [
     "GqaError", "lib", "gqa_decode", "nvfp4_paged_ctx_attn", "gqa_debug_dequant_pages",
-    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_paged", "gqa_debug_wait_expiry", "gqa_decode_noalloc", "gqa_debug_starve_producers", "gqa_set_schedule", "LIB_PATH",
+    "gqa_check_device_errors", "gqa_release_workspace", "gqa_decode_plan", "gqa_ctx_plan", "gqa_decode_paged", "gqa_debug_wait_expiry", "gqa_decode_noalloc", "gqa_debug_starve_producers", "gqa_set_schedule", "gqa_set_ctx_grid", "LIB_PATH",
     "build",
 ]
 
@@ -113,7 +113,7 @@ def lib() -> ctypes.CDLL:
                                           c.POINTER(c.c_int32)]
             L.gqa_decode_plan.restype = c.c_int
             L.gqa_ctx_plan.argtypes = [i64, i64, i64, c.POINTER(c.c_int32), c.POINTER(c.c_int32),
-                                       c.POINTER(c.c_int32)]
+                                       c.POINTER(c.c_int32), c.POINTER(c.c_int32)]
             L.gqa_ctx_plan.restype = c.c_int
             L.gqa_decode_paged.argtypes = [vp, vp, vp, i32p, i32p, vp, i64, i64, i64, f32, vp]
             L.gqa_decode_paged.restype = c.c_int
@@ -123,7 +123,8 @@ def lib() -> ctypes.CDLL:
             L.gqa_debug_starve_producers.restype = c.c_int
             L.gqa_set_schedule.argtypes = [c.c_int, c.c_int, c.c_int]
             L.gqa_set_schedule.restype = c.c_int
-            L.gqa_debug_starve_producers.restype = c.c_int
+            L.gqa_set_ctx_grid.argtypes = [c.c_int]
+            L.gqa_set_ctx_grid.restype = c.c_int
             L.gqa_release_workspace.argtypes = []
             L.gqa_release_workspace.restype = c.c_int
             _lib = L
@@ -249,11 +250,11 @@ def gqa_decode_plan(batch: int, capacity: int) -> dict:
 
 
 def gqa_ctx_plan(batch: int, total_q: int, max_pages_per_seq: int) -> dict:
-    """tiles_per_split, num_splits and num_launches of an nvfp4_paged_ctx_attn call."""
-    t, n, l = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    """tiles_per_split, num_splits, num_launches and persistent (grid) of an nvfp4_paged_ctx_attn call."""
+    t, n, l, p = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     _check(lib().gqa_ctx_plan(int(batch), int(total_q), int(max_pages_per_seq), ctypes.byref(t), ctypes.byref(n),
-                              ctypes.byref(l)))
-    return {"tiles_per_split": t.value, "num_splits": n.value, "num_launches": l.value}
+                              ctypes.byref(l), ctypes.byref(p)))
+    return {"tiles_per_split": t.value, "num_splits": n.value, "num_launches": l.value, "persistent": p.value}
 
 
 def gqa_debug_wait_expiry(device: int = 0) -> None:
@@ -269,6 +270,15 @@ def gqa_debug_starve_producers(enable: bool) -> None:
     consumer's bounded wait expires (~2 s); enable=False restores normal
     operation."""
     _check(lib().gqa_debug_starve_producers(1 if enable else 0))
+
+
+CTX_GRID_PLANNED, CTX_GRID_PER_UNIT, CTX_GRID_PERSISTENT = 0, 1, 2
+
+
+def gqa_set_ctx_grid(mode: int) -> None:
+    """Grid of later unsplit context calls (process-wide test switch, see
+    include/gqa.h): 0 as planned, 1 one CTA per unit, 2 persistent."""
+    _check(lib().gqa_set_ctx_grid(int(mode)))
 
 
 def gqa_set_schedule(ctx_packed_stages: int = 0, ctx_kv_slots: int = 0, decode_stages: int = 0) -> None:

@@ -249,7 +249,7 @@ gqa_status check_devices(std::initializer_list<std::pair<const gqa_tensor*, cons
   } while (0)
 
 std::atomic<int> g_starve{0};
-std::atomic<int> g_ctx_stages{0}, g_ctx_slots{0}, g_decode_stages{0};
+std::atomic<int> g_ctx_stages{0}, g_ctx_slots{0}, g_decode_stages{0}, g_ctx_grid{0};
 
 }  // namespace
 
@@ -258,13 +258,14 @@ int starve_producers() { return g_starve.load(std::memory_order_relaxed); }
 int schedule_ctx_stages() { return g_ctx_stages.load(std::memory_order_relaxed); }
 int schedule_ctx_slots() { return g_ctx_slots.load(std::memory_order_relaxed); }
 int schedule_decode_stages() { return g_decode_stages.load(std::memory_order_relaxed); }
+int schedule_ctx_grid() { return g_ctx_grid.load(std::memory_order_relaxed); }
 }  // namespace gqa
 
 extern "C" {
 
 const char* gqa_last_error(void) { return t_last_error.c_str(); }
 
-int gqa_version(void) { return 300; }  // 0.3.0: qo_indptr checked on the device, gqa_debug_starve_producers
+int gqa_version(void) { return 301; }  // 0.3.1: persistent context grid, gqa_set_ctx_grid, gqa_ctx_plan(persistent)
 
 namespace {
 gqa_status decode_impl(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
@@ -460,7 +461,7 @@ gqa_status gqa_decode_plan(int64_t batch, int64_t capacity, int32_t* tokens_per_
 }
 
 gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_seq, int32_t* tiles_per_split,
-                        int32_t* num_splits, int32_t* num_launches) {
+                        int32_t* num_splits, int32_t* num_launches, int32_t* persistent) {
   if (batch < 1 || batch > (1 << 20)) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 2^20]", (long long)batch);
   if (total_q < 0 || total_q > 2147483647LL) return fail(GQA_ERR_INVALID_ARG, "total_q %lld out of range", (long long)total_q);
   if (max_pages_per_seq < 1 || max_pages_per_seq > (2147483647LL / 64))
@@ -469,6 +470,7 @@ gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_se
   if (tiles_per_split) *tiles_per_split = plan.tiles_per_split;
   if (num_splits) *num_splits = plan.n_splits;
   if (num_launches) *num_launches = total_q == 0 ? 0 : (plan.n_splits > 1 ? 2 : 1);
+  if (persistent) *persistent = total_q > 0 && plan.n_splits == 1 && plan.persistent ? 1 : 0;
   return GQA_OK;
 }
 
@@ -633,6 +635,13 @@ gqa_status gqa_set_schedule(int ctx_packed_stages, int ctx_kv_slots, int decode_
   g_ctx_stages.store(ctx_packed_stages, std::memory_order_relaxed);
   g_ctx_slots.store(ctx_kv_slots, std::memory_order_relaxed);
   g_decode_stages.store(decode_stages, std::memory_order_relaxed);
+  return GQA_OK;
+}
+
+gqa_status gqa_set_ctx_grid(int mode) {
+  if (mode < GQA_CTX_GRID_PLANNED || mode > GQA_CTX_GRID_PERSISTENT)
+    return fail(GQA_ERR_INVALID_ARG, "context grid mode %d is not 0, 1 or 2", mode);
+  g_ctx_grid.store(mode, std::memory_order_relaxed);
   return GQA_OK;
 }
 

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "ctx_kernel.cuh"
+#include "ctx_persistent.cuh"
 
 namespace gqa {
 using namespace ctx;
@@ -73,6 +74,12 @@ __global__ void dequant_pages_kernel(const uint8_t* __restrict__ fp4, const uint
 constexpr int kMergeWarps = 8;
 constexpr int kCtxSplitTargetCtas = 152;  // one wave: one CTA per SM
 constexpr int kMinTilesPerSplit = 8;      // a split amortises the CTA's start-up over >= 512 keys
+// The persistent grid pays when units are short: it saves ~3 us of CTA start
+// and end per unit and computes a tile ~8 % (~0.06 us) slower, so it breaks
+// even near 47 tiles per unit.  Taken when every unit has at most 48 tiles
+// (max_pages_per_seq <= 48) and there are at least two units per SM.
+constexpr int64_t kPersistentMaxPages = 48;
+constexpr int64_t kPersistentMinUnits = 2 * kCtxSplitTargetCtas;
 
 __global__ void __launch_bounds__(32 * kMergeWarps)
     ctx_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml, uint8_t* __restrict__ out,
@@ -168,10 +175,11 @@ static int64_t max_query_blocks(int64_t batch, int64_t total_q) {
 }
 
 CtxPlan plan_ctx(int64_t batch, int64_t total_q, int64_t max_pages_per_seq) {
-  CtxPlan p{0, 1};
+  CtxPlan p{0, 1, 0};
   if (batch < 1 || total_q < 1 || max_pages_per_seq < 1) return p;
   // Launched units (an upper bound on the real ones, as the grid below).
   const int64_t units = max_query_blocks(batch, total_q) * kHkv;
+  p.persistent = units >= kPersistentMinUnits && max_pages_per_seq <= kPersistentMaxPages;
   int64_t splits = kCtxSplitTargetCtas / units;
   const int64_t by_len = max_pages_per_seq / kMinTilesPerSplit;
   if (by_len < splits) splits = by_len;
@@ -200,6 +208,9 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
     if ((st && st != kCtxStagesDefault) || (sl && sl != kCtxSlotsDefault))
       return launch_ctx_study(a, q_map, (unsigned)grid, scale_log2, inv_out_scale, st ? st : kCtxStagesDefault,
                               sl ? sl : kCtxSlotsDefault, stream);
+    const int mode = schedule_ctx_grid();
+    if (mode == 2 || (mode == 0 && plan.persistent))
+      return launch_persistent<kCtxStagesDefault, kCtxSlotsDefault>(a, q_map, grid, scale_log2, inv_out_scale, stream);
     return launch_attention<false, kCtxStagesDefault, kCtxSlotsDefault>(
         a, q_map, dim3((unsigned)grid, 1), scale_log2, inv_out_scale, 0, nullptr, nullptr, stream);
   }

@@ -22,6 +22,8 @@ int starve_producers();
 int schedule_ctx_stages();
 int schedule_ctx_slots();
 int schedule_decode_stages();
+// Grid of unsplit context calls: 0 = as planned, 1 = one CTA per unit, 2 = persistent.
+int schedule_ctx_grid();
 bool ctx_schedule_supported(int stages, int slots);
 bool decode_schedule_supported(int stages);
 
@@ -110,6 +112,7 @@ struct CtxArgs {
 struct CtxPlan {
   int tiles_per_split;  // 64-key tiles per split CTA (0 when n_splits == 1)
   int n_splits;         // 1: the attention kernel writes the output itself
+  int persistent;       // unsplit calls of short units: the persistent grid (one CTA per SM walks its units)
 };
 
 CtxPlan plan_ctx(int64_t batch, int64_t total_q, int64_t max_pages_per_seq);

@@ -287,11 +287,26 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
  * call (0 when total_q = 0; 1 unsplit; 2 with the merge).  The split is used
  * when at most 76 units (8 KV heads x floor((total_q + 63 * batch) / 64), a
  * bound on the (sequence, 64-query block) pairs) can be launched and every
- * range keeps at least 8 tiles.  Any output pointer may be
- * NULL.
+ * range keeps at least 8 tiles.  *persistent = 1 when an unsplit call runs
+ * the persistent grid (one CTA per SM walks a share of the units; same
+ * result, bit for bit): at least 304 units and max_pages_per_seq <= 48, i.e.
+ * short units, whose per-CTA start and end it saves.  Any output pointer may
+ * be NULL.
  */
 gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_seq, int32_t* tiles_per_split,
-                        int32_t* num_splits, int32_t* num_launches);
+                        int32_t* num_splits, int32_t* num_launches, int32_t* persistent);
+
+/*
+ * gqa_set_ctx_grid -- test switch: the grid of later unsplit
+ * nvfp4_paged_ctx_attn calls (all devices, all threads; process-wide).
+ * GQA_CTX_GRID_PLANNED (0) = as gqa_ctx_plan reports; GQA_CTX_GRID_PER_UNIT
+ * (1) = one CTA per work unit; GQA_CTX_GRID_PERSISTENT (2) = the persistent
+ * grid.  Both grids compute the same result, bit for bit; split-KV calls and
+ * the ring-depth study instances (gqa_set_schedule) always run one CTA per
+ * unit.  GQA_ERR_INVALID_ARG for another mode (nothing changes).
+ */
+enum { GQA_CTX_GRID_PLANNED = 0, GQA_CTX_GRID_PER_UNIT = 1, GQA_CTX_GRID_PERSISTENT = 2 };
+gqa_status gqa_set_ctx_grid(int mode);
 
 /*
  * gqa_debug_dequant_pages -- test export of the context kernel's NVFP4 ->

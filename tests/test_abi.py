@@ -233,11 +233,37 @@ def test_ctx_plan_splits_only_small_calls():
             assert p["tiles_per_split"] >= 8
             assert p["num_splits"] * p["tiles_per_split"] >= mp        # the ranges cover every tile
             assert (p["num_splits"] - 1) * p["tiles_per_split"] < mp   # and none lies past the table
-    assert gqa.gqa_ctx_plan(2, 2, 64) == {"tiles_per_split": 8, "num_splits": 8, "num_launches": 2}
-    assert gqa.gqa_ctx_plan(1, 32, 512) == {"tiles_per_split": 27, "num_splits": 19, "num_launches": 2}
+    assert gqa.gqa_ctx_plan(2, 2, 64) == {"tiles_per_split": 8, "num_splits": 8, "num_launches": 2, "persistent": 0}
+    assert gqa.gqa_ctx_plan(1, 32, 512) == {"tiles_per_split": 27, "num_splits": 19, "num_launches": 2,
+                                            "persistent": 0}
     assert gqa.gqa_ctx_plan(1, 0, 16)["num_launches"] == 0
     with pytest.raises(gqa.GqaError):
         gqa.gqa_ctx_plan(0, 1, 16)
+
+
+def test_ctx_plan_takes_persistent_grid_only_for_many_short_units():
+    """Unsplit calls with at least two units per SM (8 x floor((total_q + 63
+    batch) / 64) >= 304) and short units (max_pages_per_seq <= 48) run the
+    persistent grid; long units, few units and split calls do not."""
+    assert gqa.gqa_ctx_plan(4, 8192, 32)["persistent"] == 1     # ctx_b4_q2048_kv2048
+    assert gqa.gqa_ctx_plan(2, 8192, 1024)["persistent"] == 0   # ctx_b2_q4096_kv65536: long units
+    assert gqa.gqa_ctx_plan(64, 64, 128)["persistent"] == 0     # decode-shaped, 128 tiles per unit
+    assert gqa.gqa_ctx_plan(1, 2369, 48)["persistent"] == 1  # 8 x floor(2432 / 64) = 304 units, 48 pages
+    assert gqa.gqa_ctx_plan(1, 2369, 49)["persistent"] == 0
+    assert gqa.gqa_ctx_plan(1, 2368, 48)["persistent"] == 0  # 296 units
+    assert gqa.gqa_ctx_plan(1, 0, 16)["persistent"] == 0
+    for B, tq, mp in [(2, 2, 64), (1, 32, 512), (1, 1, 4), (3, 5, 5)]:
+        p = gqa.gqa_ctx_plan(B, tq, mp)
+        assert not (p["persistent"] and p["num_splits"] > 1)
+
+
+def test_ctx_grid_switch_validates(L):
+    for mode in (2, 1, 0):
+        assert L.gqa_set_ctx_grid(mode) == OK
+    assert L.gqa_set_ctx_grid(3) == INVALID
+    assert L.gqa_set_ctx_grid(-1) == INVALID
+    assert b"grid mode" in L.gqa_last_error()
+    assert L.gqa_set_ctx_grid(0) == OK
 
 
 def test_starvation_switch_toggles(L):
