@@ -70,11 +70,12 @@ FP8_OVER_BF16 = 2.0        # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal: a read-only stream may exceed the measured copy figure
 # Committed ncu summaries: DRAM bytes per launch, valid while the kernel source digest matches.
 _DEC_SRC = ["decode.cu", "common.cuh", "kernels.h"]
-_CTX_SRC = ["ctx_kernel.cuh", "ctx_nvfp4.cu", "common.cuh", "nvfp4.cuh", "tcgen05.cuh", "kernels.h"]
+_CTX_SRC = ["ctx_kernel.cuh", "ctx_persistent.cuh", "ctx_nvfp4.cu", "common.cuh", "nvfp4.cuh", "tcgen05.cuh",
+            "kernels.h"]
 PROFILES = {
     "decode_b64_cap8192": ("decode_split_kernel_decode_b64_cap8192.md", _DEC_SRC),
     "decode_b8_cap131072": ("decode_split_kernel_decode_b8_cap131072.md", _DEC_SRC),
-    "ctx_b4_q2048_kv2048": ("ctx_nvfp4_kernel_ctx_b4_q2048_kv2048.md", _CTX_SRC),
+    "ctx_b4_q2048_kv2048": ("ctx_nvfp4_persistent_kernel_ctx_b4_q2048_kv2048.md", _CTX_SRC),
     "ctx_b2_q4096_kv65536": ("ctx_nvfp4_kernel_ctx_b2_q4096_kv65536.md", _CTX_SRC),
 }
 
@@ -311,6 +312,15 @@ class Workload:
         else:
             self.gqa.nvfp4_paged_ctx_attn(*self.args, q_scale=x.q_scale, out_scale=x.out_scale, out=self.out)
 
+    @property
+    def kernel(self):
+        """The attention kernel(s) one call launches, as the launch plan chooses them."""
+        if self.kind == "decode":
+            return "decode_split_kernel" + (" + decode_merge_kernel" if self.launches > 1 else "")
+        if self.plan.get("persistent") and self.launches == 1:
+            return "ctx_nvfp4_persistent_kernel"
+        return "ctx_nvfp4_kernel" + (" + ctx_merge_kernel" if self.launches > 1 else "")
+
     def rate(self, ms):
         """GB/s (decode) or TFLOP/s (ctx) for one call of `ms` milliseconds."""
         return self.work / (ms * 1e-3) / (1e9 if self.kind == "decode" else 1e12)
@@ -329,8 +339,7 @@ class Workload:
                     "peak_nominal": HBM_NOMINAL_GBS, "frac_nominal": round(a / HBM_NOMINAL_GBS, 4),
                     "traffic": traffic, "traffic_source": src,
                     "algorithmic": f"{self.work} B = sum of lengths x 4096 B (K+V, 8 heads x 128 x fp16)",
-                    "kernel": ("decode_split_kernel" + (" + decode_merge_kernel" if self.launches > 1 else "")
-                               + " inside the same events")}
+                    "kernel": self.kernel + " inside the same events"}
         fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
         if self.name in MEMORY_BOUND_CTX:
             # decode-shaped: a few query rows per KV head, so the page bytes, not the tensor work, bound it
@@ -340,13 +349,13 @@ class Workload:
                     "frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4),
                     "algorithmic": f"{self.x.page_bytes_read()} B = every used page's packed codes and scales, "
                                    "K and V, once", "tflops": round(a, 2),
-                    "kernel": "ctx_nvfp4_kernel" + (" + ctx_merge_kernel" if self.launches > 1 else "")}
+                    "kernel": self.kernel}
         return {"bound": "tensor", "achieved": round(a, 2), "peak": round(fp8, 1), "unit": "TFLOP/s",
                 "frac": round(a / fp8, 4),
                 "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16} (nominal dense FP8:bf16)",
                 "traffic": traffic, "traffic_source": src,
                 "algorithmic": f"{self.work} FLOP = 4 x 128 x 32 heads x visible (query, key) pairs",
-                "kernel": "ctx_nvfp4_kernel" + (" + ctx_merge_kernel" if self.launches > 1 else "")}
+                "kernel": self.kernel}
 
     def config(self):
         x = self.x
