@@ -493,8 +493,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // partial sum is inf and fails the test).  Otherwise (a row's first
         // keys, where m_used is -inf, or a maximum that grew by more than ~9) the
         // warp finds the rows' maxima, raises m where it grew by more than
-        // 2^kRescaleLog2 (rescaling O and l), and computes P again.
-        float lsum = mask_warp ? pass_p(std::true_type{}) : pass_p(std::false_type{});
+        // 2^kRescaleLog2 (rescaling O and l), and computes P again.  The
+        // optimistic pass is skipped where it is bound to fail: a row whose
+        // m_used is still -inf and which sees a key of this tile gets an
+        // infinite weight (the same P results either way).
+        float lsum = INFINITY;
+        if (!__any_sync(0xffffffffu, m_used == -INFINITY && kbase <= lim_key))
+          lsum = mask_warp ? pass_p(std::true_type{}) : pass_p(std::false_type{});
         if (__any_sync(0xffffffffu, !(lsum <= kMaxTileSum))) {
           // extreme raw logit of the row (max, or min for a negative scale),
           // then the scaled maximum in the exp2 domain
