@@ -109,8 +109,7 @@ struct Smem {
   uint64_t p_full[2][2], p_free[2][2];    // [M-tile][buffer]: P written / the P V that read it completed
   uint64_t q_ready, o_final[2];           // Q loaded; every MMA of M-tile T complete
   uint64_t drain[3];                // teardown after an expired wait: MMAs of issuer warps 1..3 complete
-  uint2 ktab[256];                  // E4M3 magnitudes of the 8 E2M1 codes for every scale byte
-  uint4 vtab[256];                  // the same values as f16 byte tables
+  uint2 ktab[256];                  // E4M3 magnitudes of the 8 E2M1 codes for every scale byte (K and V)
   uint32_t tmem_base;
   int unit_b, unit_qb;
 };
@@ -266,9 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   for (int i = threadIdx.x; i < 256; i += kThreads) {
-    const uint2 t = nvfp4_scale_table((uint32_t)i);
-    sm.ktab[i] = t;
-    sm.vtab[i] = nvfp4_f16_table(t);
+    sm.ktab[i] = nvfp4_scale_table((uint32_t)i);
   }
   if (threadIdx.x == 32) {
     for (int i = 0; i < kNP; ++i) {
@@ -705,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint4 packed[2][2];
       uint2 ktab[2][2];
-      uint4 vtab[2][2];
+      uint2 vtab[2][2];
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
         const int key = key0 + 32 * it;
@@ -715,8 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vs = *reinterpret_cast<const uint16_t*>(&sm.sf[st][1][key * 8 + pb * 2]);
         ktab[it][0] = sm.ktab[ks & 0xffu];
         ktab[it][1] = sm.ktab[ks >> 8];
-        vtab[it][0] = sm.vtab[vs & 0xffu];
-        vtab[it][1] = sm.vtab[vs >> 8];
+        vtab[it][0] = sm.ktab[vs & 0xffu];
+        vtab[it][1] = sm.ktab[vs >> 8];
       }
       if (j >= kNK && !mbar_wait(smem_u32(&sm.kv_free[slot]), ((j / kNK) - 1) & 1, &g_ctx_err)) {
         ok = false;

@@ -49,12 +49,15 @@ __global__ void dequant_pages_kernel(const uint8_t* __restrict__ fp4, const uint
       r = dequant16_e4m3(packed, tab);
       if ((sfb & 0x7fu) != 0x7fu) {  // (a NaN scale has no numbers to compare)
         const uint4 vt = nvfp4_f16_table(tab);
-        const uint4 h0 = nvfp4_to_f16_8(packed.x, vt), h1 = nvfp4_to_f16_8(packed.y, vt);
+        const uint4 h0 = nvfp4_to_f16_8(packed.x, tab), h1 = nvfp4_to_f16_8(packed.y, tab);
+        const uint4 t0 = nvfp4_to_f16_8_tables(packed.x, vt), t1 = nvfp4_to_f16_8_tables(packed.y, vt);
         const uint32_t e[4] = {f16x2_to_e4m3x2(h0.x) | (f16x2_to_e4m3x2(h0.y) << 16),
                                f16x2_to_e4m3x2(h0.z) | (f16x2_to_e4m3x2(h0.w) << 16),
                                f16x2_to_e4m3x2(h1.x) | (f16x2_to_e4m3x2(h1.y) << 16),
                                f16x2_to_e4m3x2(h1.z) | (f16x2_to_e4m3x2(h1.w) << 16)};
-        if (e[0] != r.x || e[1] != r.y || e[2] != r.z || e[3] != r.w) atomicOr(&g_ctx_err, kErrSelfCheck);
+        const bool same = h0.x == t0.x && h0.y == t0.y && h0.z == t0.z && h0.w == t0.w && h1.x == t1.x &&
+                          h1.y == t1.y && h1.z == t1.z && h1.w == t1.w;
+        if (!same || e[0] != r.x || e[1] != r.y || e[2] != r.z || e[3] != r.w) atomicOr(&g_ctx_err, kErrSelfCheck);
       }
     } else {
       atomicOr(&g_ctx_err, kErrBadIndex);

@@ -61,8 +61,7 @@ struct PSmem {
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];  // descriptor written / read by all 15 consumer warps
   uint64_t drain[3];                // teardown after an expired wait: MMAs of issuer warps 1..3 complete
   Unit unit[kUnitRing];
-  uint2 ktab[256];                  // E4M3 magnitudes of the 8 E2M1 codes for every scale byte
-  uint4 vtab[256];                  // the same values as f16 byte tables
+  uint2 ktab[256];                  // E4M3 magnitudes of the 8 E2M1 codes for every scale byte (K and V)
   uint32_t tmem_base;
 };
 
@@ -144,9 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   for (int i = threadIdx.x; i < 256; i += kThreads) {
-    const uint2 t = nvfp4_scale_table((uint32_t)i);
-    sm.ktab[i] = t;
-    sm.vtab[i] = nvfp4_f16_table(t);
+    sm.ktab[i] = nvfp4_scale_table((uint32_t)i);
   }
   if (threadIdx.x == 32) {
     for (int i = 0; i < kNP; ++i) {
@@ -642,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint4 packed[2][2];
         uint2 ktab[2][2];
-        uint4 vtab[2][2];
+        uint2 vtab[2][2];
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
           const int key = key0 + 32 * it;
@@ -652,8 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vs = *reinterpret_cast<const uint16_t*>(&sm.sf[st][1][key * 8 + pb * 2]);
           ktab[it][0] = sm.ktab[ks & 0xffu];
           ktab[it][1] = sm.ktab[ks >> 8];
-          vtab[it][0] = sm.vtab[vs & 0xffu];
-          vtab[it][1] = sm.vtab[vs >> 8];
+          vtab[it][0] = sm.ktab[vs & 0xffu];
+          vtab[it][1] = sm.ktab[vs >> 8];
         }
         if (gt >= kNK && !wait_all(&sm.kv_free[slot], ((gt / kNK) - 1) & 1)) {
           ok = false;

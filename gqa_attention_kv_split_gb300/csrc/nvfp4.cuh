@@ -15,9 +15,11 @@
 // sign bit of the result (a flip, not a set: the scale may be negative).
 //
 // Two outputs per code word: E4M3 bytes (the K tile of S = Q K^T) and the
-// same values widened to f16 (the V tile of the f16 P V product), the latter
-// looked up directly from a table of the f16 encodings of the E4M3 values,
-// so both are the same E4M3 numbers bit for bit.
+// same values widened to f16 (the V tile of the f16 P V product) by the
+// hardware's exact E4M3 -> f16 conversion of those bytes, so both are the same
+// E4M3 numbers bit for bit.  (A second f16 construction, straight from byte
+// tables of the f16 encodings, serves as the device-side cross-check of the
+// dequantisation test export.)
 #pragma once
 #include <cstdint>
 
@@ -88,8 +90,17 @@ __device__ __forceinline__ uint2 nvfp4_to_e4m3_8(uint32_t w, uint2 tab) {
 }
 
 // 8 codes -> 8 f16 values of the E4M3 results, as 4 f16x2 words (element 2i
-// in the low half of word i).
-__device__ __forceinline__ uint4 nvfp4_to_f16_8(uint32_t w, uint4 tab) {
+// in the low half of word i): the E4M3 bytes, then the exact conversion.
+__device__ __forceinline__ uint4 nvfp4_to_f16_8(uint32_t w, uint2 tab) {
+  const uint2 e = nvfp4_to_e4m3_8(w, tab);
+  return make_uint4(e4m3x2_to_f16x2(e.x & 0xffffu), e4m3x2_to_f16x2(e.x >> 16), e4m3x2_to_f16x2(e.y & 0xffffu),
+                    e4m3x2_to_f16x2(e.y >> 16));
+}
+
+// The same 8 f16 values built from the f16 byte tables of nvfp4_f16_table
+// (no conversion instruction): the independent construction the test export
+// checks nvfp4_to_f16_8 against.
+__device__ __forceinline__ uint4 nvfp4_to_f16_8_tables(uint32_t w, uint4 tab) {
   const uint32_t wm = w & 0x77777777u;
   const uint32_t wmh = wm >> 16;
   const uint2 sg = nvfp4_sign_bytes(w);
