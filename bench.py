@@ -588,9 +588,11 @@ def run_study(args):
     gqa.lib()
     stream = torch.cuda.current_stream(dev)
     flush = L2Flush(torch, dev)
-    names = [args.workload] if args.workload else ["ctx_b2_q4096_kv65536", "ctx_b4_q2048_kv2048",
+    names = [args.workload] if args.workload else ["ctx_b2_q4096_kv65536", "ctx_b4_q2048_kv2048", "ctx_b64_q1_kv8192",
                                                    "decode_b8_cap131072", "decode_b64_cap8192"]
     rows = []
+    # every ring depth on the same grid: the study instances run one CTA per unit, so the production depths do too
+    gqa.gqa_set_ctx_grid(gqa.CTX_GRID_PER_UNIT)
     with ClockSampler(0) as clk:
         time.sleep(0.3)
         clk.mark("start")
@@ -630,7 +632,9 @@ def run_study(args):
             del wl
             torch.cuda.empty_cache()
         clk.mark("stop")
-    print(json.dumps({"study": "ring depths (gqa_set_schedule)", "rows": rows, "clocks": clk.summary()}), flush=True)
+    gqa.gqa_set_ctx_grid(gqa.CTX_GRID_PLANNED)
+    print(json.dumps({"study": "ring depths (gqa_set_schedule), context calls on the one-CTA-per-unit grid",
+                      "rows": rows, "clocks": clk.summary()}), flush=True)
 
 
 # ---------------------------------------------------------- oracle (CPU) --

@@ -287,7 +287,8 @@ def gqa_set_schedule(ctx_packed_stages: int = 0, ctx_kv_slots: int = 0, decode_s
     _check(lib().gqa_set_schedule(int(ctx_packed_stages), int(ctx_kv_slots), int(decode_stages)))
 
 
-CTX_SCHEDULES = [(6, 4), (4, 4), (8, 4), (10, 4), (6, 3), (12, 3), (6, 5), (6, 2)]
+# the production depths first: (4, 4) for the one-CTA-per-unit context kernel, decode depth 8
+CTX_SCHEDULES = [(4, 4), (6, 4), (8, 4), (10, 4), (6, 3), (12, 3), (6, 5), (6, 2)]
 DECODE_SCHEDULES = [8, 4, 12, 16]
 
 

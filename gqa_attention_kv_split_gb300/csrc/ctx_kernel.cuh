@@ -88,8 +88,14 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemPerTile = 256;
 constexpr uint32_t kTmemSP = 64;  // columns per S/P buffer
 constexpr uint32_t kTmemO = 128;
-// Ring depths of the production instances: packed-page stages and dequantised K/V slots.
-constexpr int kCtxStagesDefault = 6;
+// Ring depths of the production instances (packed-page stages, dequantised
+// K/V slots), chosen by the ring-depth study (interleaved timing, outputs
+// byte-identical at every depth): the one-CTA-per-unit kernel of unsplit
+// calls runs 4 stages (1.6-2.4 % ahead of 6 on long units); the persistent
+// grid (0.9 % ahead at 6) and split-KV calls (no difference) run 6.
+constexpr int kCtxStagesDefault = 4;
+constexpr int kCtxStagesPersistent = 6;
+constexpr int kCtxStagesSplit = 6;
 constexpr int kCtxSlotsDefault = 4;
 
 // Error word of the context kernels of one translation unit (bitwise OR of

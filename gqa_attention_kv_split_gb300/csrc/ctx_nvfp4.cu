@@ -213,7 +213,8 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
                               sl ? sl : kCtxSlotsDefault, stream);
     const int mode = schedule_ctx_grid();
     if (mode == 2 || (mode == 0 && plan.persistent))
-      return launch_persistent<kCtxStagesDefault, kCtxSlotsDefault>(a, q_map, grid, scale_log2, inv_out_scale, stream);
+      return launch_persistent<kCtxStagesPersistent, kCtxSlotsDefault>(a, q_map, grid, scale_log2, inv_out_scale,
+                                                                          stream);
     return launch_attention<false, kCtxStagesDefault, kCtxSlotsDefault>(
         a, q_map, dim3((unsigned)grid, 1), scale_log2, inv_out_scale, 0, nullptr, nullptr, stream);
   }
@@ -222,7 +223,7 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
   const int64_t rows = a.total_q * kHq;
   float* part_o = static_cast<float*>(workspace);
   float2* part_ml = reinterpret_cast<float2*>(part_o + (size_t)plan.n_splits * rows * kD);
-  e = launch_attention<true, kCtxStagesDefault, kCtxSlotsDefault>(
+  e = launch_attention<true, kCtxStagesSplit, kCtxSlotsDefault>(
       a, q_map, dim3((unsigned)grid, (unsigned)plan.n_splits), scale_log2, inv_out_scale, plan.tiles_per_split,
       part_o, part_ml, stream);
   if (e != cudaSuccess) return e;

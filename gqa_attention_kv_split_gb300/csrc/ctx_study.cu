@@ -24,7 +24,7 @@ cudaError_t launch_ctx_study(const CtxArgs& a, const CUtensorMap& q_map, unsigne
                              float inv_out_scale, int stages, int slots, cudaStream_t stream) {
   const dim3 g(grid, 1);
   switch (stages * 100 + slots) {
-    case 404: return ctx::launch_attention<false, 4, 4>(a, q_map, g, scale_log2, inv_out_scale, 0, nullptr, nullptr, stream);
+    case 604: return ctx::launch_attention<false, 6, 4>(a, q_map, g, scale_log2, inv_out_scale, 0, nullptr, nullptr, stream);
     case 804: return ctx::launch_attention<false, 8, 4>(a, q_map, g, scale_log2, inv_out_scale, 0, nullptr, nullptr, stream);
     case 1004: return ctx::launch_attention<false, 10, 4>(a, q_map, g, scale_log2, inv_out_scale, 0, nullptr, nullptr, stream);
     case 603: return ctx::launch_attention<false, 6, 3>(a, q_map, g, scale_log2, inv_out_scale, 0, nullptr, nullptr, stream);

@@ -355,10 +355,12 @@ gqa_status gqa_debug_wait_expiry(int device, gqa_stream_t stream);
  * and its results section) -- so a schedule changes only speed.
  *
  *   ctx_packed_stages, ctx_kv_slots  packed NVFP4 page stages and dequantised
- *       K/V tile slots of the (unsplit) context attention kernel; 0 = the
- *       production depth (6 stages, 4 slots).  Instantiated (stages, slots):
- *       (6,4) (4,4) (8,4) (10,4) (6,3) (12,3) (6,5) (6,2).  Split-KV calls
- *       always run the production depths.
+ *       K/V tile slots of the one-CTA-per-unit context attention kernel of
+ *       unsplit calls; 0 = its production depth (4 stages, 4 slots).
+ *       Instantiated (stages, slots): (4,4) (6,4) (8,4) (10,4) (6,3) (12,3)
+ *       (6,5) (6,2).  A non-production depth runs every unsplit call on the
+ *       one-CTA-per-unit grid; split-KV calls and the persistent grid always
+ *       run their production depths (6 stages, 4 slots).
  *   decode_stages  16-token K/V stages of the decode ring (stacked cache);
  *       0 = the production depth 8; also 4, 12, 16.  The paged decode always
  *       runs depth 8.
