@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (!ok) failed = true;
     }
-  } else if (warp < 12) {
+  } else if (warp < 8 || (warp < 12 && t1_live)) {
     // -------------------------------------------------------------- softmax
     const int T = (warp - 4) >> 2;
     const int sub = warp & 3;
@@ -692,14 +692,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stage), so their latencies overlap one another and the wait; K and V
     // are then written and published together.  Keys past kv_len (only in a
     // sequence's last tile) read as zero.
-    const int dt = threadIdx.x - 384;
+    // Warps 12-15 dequantise every tile; when M-tile 1 is idle its softmax
+    // warps 8-11 form a second group: group 0 takes the even tiles, group 1
+    // the odd ones, so two tiles' chains (page wait, loads, table lookups,
+    // conversion, slot wait, stores, publication) overlap -- a tile's chain,
+    // not the dequantisers' issue rate, bounds the one-M-tile calls.  Each
+    // tile is still written and published by one group of four warps.
+    const int group = warp >= 12 ? 0 : 1;
+    const int j_step = t1_live ? 1 : 2;
+    const int dt = (threadIdx.x & 127);
     const int key0 = dt >> 2;  // items dt + 128 it: key = key0 + 32 it, block pair pb = dt & 3
     const int pb = dt & 3;
     // V: blocks 2 pb and 2 pb + 1 are d = 32 pb .. 32 pb + 31, i.e. half pb / 2,
     // 16-byte chunks 4 (pb % 2) .. 4 (pb % 2) + 3
     const int vc0 = 4 * (pb & 1);
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = group; j < n_tiles; j += j_step) {
       const int st = j % kNP;
       const int slot = j % kNK;
       if (!mbar_wait(smem_u32(&sm.pk_full[st]), (j / kNP) & 1, &g_ctx_err)) {
