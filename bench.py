@@ -77,6 +77,7 @@ PROFILES = {
     "decode_b8_cap131072": ("decode_split_kernel_decode_b8_cap131072.md", _DEC_SRC),
     "ctx_b4_q2048_kv2048": ("ctx_nvfp4_persistent_kernel_ctx_b4_q2048_kv2048.md", _CTX_SRC),
     "ctx_b2_q4096_kv65536": ("ctx_nvfp4_kernel_ctx_b2_q4096_kv65536.md", _CTX_SRC),
+    "ctx_b64_q1_kv8192": ("ctx_nvfp4_kernel_ctx_b64_q1_kv8192.md", _CTX_SRC),
 }
 
 
@@ -346,7 +347,7 @@ class Workload:
             gbs = self.x.page_bytes_read() / (ms * 1e-3) / 1e9
             return {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_nominal": HBM_NOMINAL_GBS,
-                    "frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4),
+                    "frac_nominal": round(gbs / HBM_NOMINAL_GBS, 4), "traffic": traffic, "traffic_source": src,
                     "algorithmic": f"{self.x.page_bytes_read()} B = every used page's packed codes and scales, "
                                    "K and V, once", "tflops": round(a, 2),
                     "kernel": self.kernel}
