@@ -70,8 +70,8 @@ FP8_OVER_BF16 = 2.0        # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal: a read-only stream may exceed the measured copy figure
 # Committed ncu summaries: DRAM bytes per launch, valid while the kernel source digest matches.
 _DEC_SRC = ["decode.cu", "common.cuh", "kernels.h"]
-_CTX_SRC = ["ctx_kernel.cuh", "ctx_persistent.cuh", "ctx_nvfp4.cu", "common.cuh", "nvfp4.cuh", "tcgen05.cuh",
-            "kernels.h"]
+_CTX_SRC = ["ctx_kernel.cuh", "ctx_persistent.cuh", "ctx_decode.cuh", "ctx_nvfp4.cu", "common.cuh", "nvfp4.cuh",
+            "tcgen05.cuh", "kernels.h"]
 PROFILES = {
     "decode_b64_cap8192": ("decode_split_kernel_decode_b64_cap8192.md", _DEC_SRC),
     "decode_b8_cap131072": ("decode_split_kernel_decode_b8_cap131072.md", _DEC_SRC),
@@ -318,6 +318,8 @@ class Workload:
         """The attention kernel(s) one call launches, as the launch plan chooses them."""
         if self.kind == "decode":
             return "decode_split_kernel" + (" + decode_merge_kernel" if self.launches > 1 else "")
+        if self.plan.get("decode_shaped"):
+            return "ctx_nvfp4_decode_kernel + ctx_merge_kernel"
         if self.plan.get("persistent") and self.launches == 1:
             return "ctx_nvfp4_persistent_kernel"
         return "ctx_nvfp4_kernel" + (" + ctx_merge_kernel" if self.launches > 1 else "")

@@ -113,7 +113,7 @@ def lib() -> ctypes.CDLL:
                                           c.POINTER(c.c_int32)]
             L.gqa_decode_plan.restype = c.c_int
             L.gqa_ctx_plan.argtypes = [i64, i64, i64, c.POINTER(c.c_int32), c.POINTER(c.c_int32),
-                                       c.POINTER(c.c_int32), c.POINTER(c.c_int32)]
+                                       c.POINTER(c.c_int32), c.POINTER(c.c_int32), c.POINTER(c.c_int32)]
             L.gqa_ctx_plan.restype = c.c_int
             L.gqa_decode_paged.argtypes = [vp, vp, vp, i32p, i32p, vp, i64, i64, i64, f32, vp]
             L.gqa_decode_paged.restype = c.c_int
@@ -250,11 +250,13 @@ def gqa_decode_plan(batch: int, capacity: int) -> dict:
 
 
 def gqa_ctx_plan(batch: int, total_q: int, max_pages_per_seq: int) -> dict:
-    """tiles_per_split, num_splits, num_launches and persistent (grid) of an nvfp4_paged_ctx_attn call."""
-    t, n, l, p = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    """tiles_per_split, num_splits, num_launches and the kernel choice (persistent grid, decode-shaped
+    kernel) of an nvfp4_paged_ctx_attn call."""
+    t, n, l, p, d = (ctypes.c_int32() for _ in range(5))
     _check(lib().gqa_ctx_plan(int(batch), int(total_q), int(max_pages_per_seq), ctypes.byref(t), ctypes.byref(n),
-                              ctypes.byref(l), ctypes.byref(p)))
-    return {"tiles_per_split": t.value, "num_splits": n.value, "num_launches": l.value, "persistent": p.value}
+                              ctypes.byref(l), ctypes.byref(p), ctypes.byref(d)))
+    return {"tiles_per_split": t.value, "num_splits": n.value, "num_launches": l.value, "persistent": p.value,
+            "decode_shaped": d.value}
 
 
 def gqa_debug_wait_expiry(device: int = 0) -> None:
@@ -272,12 +274,12 @@ def gqa_debug_starve_producers(enable: bool) -> None:
     _check(lib().gqa_debug_starve_producers(1 if enable else 0))
 
 
-CTX_GRID_PLANNED, CTX_GRID_PER_UNIT, CTX_GRID_PERSISTENT = 0, 1, 2
+CTX_GRID_PLANNED, CTX_GRID_PER_UNIT, CTX_GRID_PERSISTENT, CTX_GRID_DECODE_SHAPED = 0, 1, 2, 3
 
 
 def gqa_set_ctx_grid(mode: int) -> None:
-    """Grid of later unsplit context calls (process-wide test switch, see
-    include/gqa.h): 0 as planned, 1 one CTA per unit, 2 persistent."""
+    """Grid of later context calls (process-wide test switch, see
+    include/gqa.h): 0 as planned, 1 one CTA per unit, 2 persistent, 3 decode-shaped."""
     _check(lib().gqa_set_ctx_grid(int(mode)))
 
 

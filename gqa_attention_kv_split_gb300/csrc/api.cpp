@@ -265,7 +265,7 @@ extern "C" {
 
 const char* gqa_last_error(void) { return t_last_error.c_str(); }
 
-int gqa_version(void) { return 301; }  // 0.3.1: persistent context grid, gqa_set_ctx_grid, gqa_ctx_plan(persistent)
+int gqa_version(void) { return 302; }  // 0.3.2: decode-shaped context kernel, gqa_ctx_plan(decode_shaped)
 
 namespace {
 gqa_status decode_impl(const void* q, const void* kv, const int32_t* seq_lens, void* out, int64_t batch,
@@ -461,7 +461,7 @@ gqa_status gqa_decode_plan(int64_t batch, int64_t capacity, int32_t* tokens_per_
 }
 
 gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_seq, int32_t* tiles_per_split,
-                        int32_t* num_splits, int32_t* num_launches, int32_t* persistent) {
+                        int32_t* num_splits, int32_t* num_launches, int32_t* persistent, int32_t* decode_shaped) {
   if (batch < 1 || batch > (1 << 20)) return fail(GQA_ERR_UNSUPPORTED, "batch %lld outside [1, 2^20]", (long long)batch);
   if (total_q < 0 || total_q > 2147483647LL) return fail(GQA_ERR_INVALID_ARG, "total_q %lld out of range", (long long)total_q);
   if (max_pages_per_seq < 1 || max_pages_per_seq > (2147483647LL / 64))
@@ -469,8 +469,9 @@ gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_se
   const gqa::CtxPlan plan = gqa::plan_ctx(batch, total_q, max_pages_per_seq);
   if (tiles_per_split) *tiles_per_split = plan.tiles_per_split;
   if (num_splits) *num_splits = plan.n_splits;
-  if (num_launches) *num_launches = total_q == 0 ? 0 : (plan.n_splits > 1 ? 2 : 1);
-  if (persistent) *persistent = total_q > 0 && plan.n_splits == 1 && plan.persistent ? 1 : 0;
+  if (num_launches) *num_launches = total_q == 0 ? 0 : (plan.n_splits > 1 || plan.decode_rows ? 2 : 1);
+  if (persistent) *persistent = total_q > 0 && plan.n_splits == 1 && plan.persistent && !plan.decode_rows ? 1 : 0;
+  if (decode_shaped) *decode_shaped = total_q > 0 && plan.decode_rows ? 1 : 0;
   return GQA_OK;
 }
 
@@ -639,8 +640,8 @@ gqa_status gqa_set_schedule(int ctx_packed_stages, int ctx_kv_slots, int decode_
 }
 
 gqa_status gqa_set_ctx_grid(int mode) {
-  if (mode < GQA_CTX_GRID_PLANNED || mode > GQA_CTX_GRID_PERSISTENT)
-    return fail(GQA_ERR_INVALID_ARG, "context grid mode %d is not 0, 1 or 2", mode);
+  if (mode < GQA_CTX_GRID_PLANNED || mode > GQA_CTX_GRID_DECODE_SHAPED)
+    return fail(GQA_ERR_INVALID_ARG, "context grid mode %d is not 0, 1, 2 or 3", mode);
   g_ctx_grid.store(mode, std::memory_order_relaxed);
   return GQA_OK;
 }

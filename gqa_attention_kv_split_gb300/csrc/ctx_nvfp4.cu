@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "ctx_kernel.cuh"
+#include "ctx_decode.cuh"
 #include "ctx_persistent.cuh"
 
 namespace gqa {
@@ -83,6 +84,7 @@ constexpr int kMinTilesPerSplit = 8;      // a split amortises the CTA's start-u
 // (max_pages_per_seq <= 48) and there are at least two units per SM.
 constexpr int64_t kPersistentMaxPages = 48;
 constexpr int64_t kPersistentMinUnits = 2 * kCtxSplitTargetCtas;
+constexpr int64_t kDecodeShapedMinPages = 16;
 
 __global__ void __launch_bounds__(32 * kMergeWarps)
     ctx_merge_kernel(const float* __restrict__ part_o, const float2* __restrict__ part_ml, uint8_t* __restrict__ out,
@@ -158,6 +160,26 @@ cudaError_t make_q_map(const uint8_t* q, int64_t total_q, CUtensorMap* map) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The merge of the split partials, launched as a programmatic dependent grid:
+// its launch overlaps the attention kernel's tail (it waits for that kernel
+// with griddepcontrol.wait before it reads).
+cudaError_t launch_merge(const float* part_o, const float2* part_ml, const CtxArgs& a, int64_t rows, int n_splits,
+                         float inv_out_scale, cudaStream_t stream) {
+  const int64_t mblocks = (rows + kMergeWarps - 1) / kMergeWarps;
+  if (mblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)mblocks);
+  cfg.blockDim = dim3(32 * kMergeWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ctx_merge_kernel, part_o, part_ml, a.out, rows, n_splits, inv_out_scale,
+                            a.qo_indptr, a.batch);
+}
 }  // namespace
 
 cudaError_t launch_dequant_pages(const uint8_t* fp4, const uint8_t* sf, const int32_t* block_table,
@@ -177,9 +199,36 @@ static int64_t max_query_blocks(int64_t batch, int64_t total_q) {
   return (total_q + (int64_t)(kQB - 1) * batch) / kQB;
 }
 
+// Decode-shaped plan: units of rows/4 queries per (sequence, KV head), their
+// KV ranges sized so that the units x ranges fill about four waves of the SMs
+// (fewer waves leave a costly tail, more pay the CTA start-up more often) with
+// at least 4 tiles (512 keys) per range.
+static CtxPlan plan_decode_shaped(int64_t batch, int64_t total_q, int64_t max_pages_per_seq, int rows) {
+  CtxPlan p{0, 1, 0, rows};
+  const int64_t chunk = rows / 4;
+  const int64_t units = (total_q + (chunk - 1) * batch) / chunk * kHkv;
+  const int64_t tiles = (max_pages_per_seq + 1) / 2;
+  int64_t ranges = (4 * kCtxSplitTargetCtas + units - 1) / units;
+  const int64_t by_len = tiles / 4 > 0 ? tiles / 4 : 1;
+  if (ranges > by_len) ranges = by_len;
+  if (ranges > 32) ranges = 32;  // the merge holds one range per lane
+  if (ranges < 1) ranges = 1;
+  const int64_t tpr = (tiles + ranges - 1) / ranges;
+  p.tiles_per_split = (int)tpr;
+  p.n_splits = (int)((tiles + tpr - 1) / tpr);
+  return p;
+}
+
 CtxPlan plan_ctx(int64_t batch, int64_t total_q, int64_t max_pages_per_seq) {
-  CtxPlan p{0, 1, 0};
+  CtxPlan p{0, 1, 0, 0};
   if (batch < 1 || total_q < 1 || max_pages_per_seq < 1) return p;
+  // Decode-shaped calls (at most one query per sequence on average, over at
+  // least 16 pages) take the transposed kernel, where it measured faster; a
+  // test switch forces it, and a ring-depth study keeps the prefill kernel.
+  const int mode = schedule_ctx_grid();
+  const bool study = schedule_ctx_stages() || schedule_ctx_slots();
+  if (mode == 3 || (mode == 0 && !study && total_q <= batch && max_pages_per_seq >= kDecodeShapedMinPages))
+    return plan_decode_shaped(batch, total_q, max_pages_per_seq, 16);
   // Launched units (an upper bound on the real ones, as the grid below).
   const int64_t units = max_query_blocks(batch, total_q) * kHkv;
   p.persistent = units >= kPersistentMinUnits && max_pages_per_seq <= kPersistentMaxPages;
@@ -194,7 +243,7 @@ CtxPlan plan_ctx(int64_t batch, int64_t total_q, int64_t max_pages_per_seq) {
 }
 
 size_t ctx_workspace_bytes(int64_t total_q, const CtxPlan& plan) {
-  if (plan.n_splits <= 1) return 0;
+  if (plan.n_splits <= 1 && !plan.decode_rows) return 0;
   return (size_t)plan.n_splits * (size_t)total_q * kHq * (kD * sizeof(float) + sizeof(float2));
 }
 
@@ -206,6 +255,21 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
   alignas(64) CUtensorMap q_map;
   cudaError_t e = make_q_map(a.q, a.total_q, &q_map);
   if (e != cudaSuccess) return e;
+  const int64_t rows = a.total_q * kHq;
+  if (plan.decode_rows) {
+    if (!workspace || plan.tiles_per_split < 1 || plan.n_splits < 1 || plan.n_splits > 32)
+      return cudaErrorInvalidValue;
+    const int64_t chunk = plan.decode_rows / 4;
+    const int64_t units = (a.total_q + (chunk - 1) * a.batch) / chunk * kHkv;
+    if (units <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    float* part_o = static_cast<float*>(workspace);
+    float2* part_ml = reinterpret_cast<float2*>(part_o + (size_t)plan.n_splits * rows * kD);
+    if (plan.decode_rows != 16) return cudaErrorInvalidValue;
+    e = launch_decode_shaped<16>(a, (unsigned)units, plan.n_splits, scale_log2, plan.tiles_per_split, part_o, part_ml,
+                                 stream);
+    if (e != cudaSuccess) return e;
+    return launch_merge(part_o, part_ml, a, rows, plan.n_splits, inv_out_scale, stream);
+  }
   if (plan.n_splits <= 1) {
     const int st = schedule_ctx_stages(), sl = schedule_ctx_slots();
     if ((st && st != kCtxStagesDefault) || (sl && sl != kCtxSlotsDefault))
@@ -220,29 +284,13 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
   }
   // the merge holds one range per lane
   if (!workspace || plan.tiles_per_split < 1 || plan.n_splits > 32) return cudaErrorInvalidValue;
-  const int64_t rows = a.total_q * kHq;
   float* part_o = static_cast<float*>(workspace);
   float2* part_ml = reinterpret_cast<float2*>(part_o + (size_t)plan.n_splits * rows * kD);
   e = launch_attention<true, kCtxStagesSplit, kCtxSlotsDefault>(
       a, q_map, dim3((unsigned)grid, (unsigned)plan.n_splits), scale_log2, inv_out_scale, plan.tiles_per_split,
       part_o, part_ml, stream);
   if (e != cudaSuccess) return e;
-  const int64_t mblocks = (rows + kMergeWarps - 1) / kMergeWarps;
-  if (mblocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  // programmatic dependent launch: the merge's launch overlaps the attention
-  // kernel's tail (the merge waits for it with griddepcontrol.wait)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)mblocks);
-  cfg.blockDim = dim3(32 * kMergeWarps);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, ctx_merge_kernel, (const float*)part_o, (const float2*)part_ml, a.out, rows,
-                            plan.n_splits, inv_out_scale, a.qo_indptr, a.batch);
+  return launch_merge(part_o, part_ml, a, rows, plan.n_splits, inv_out_scale, stream);
 }
 
 cudaError_t ctx_read_errors(uint32_t* word) { return read_ctx_error_word(word); }

@@ -113,6 +113,8 @@ struct CtxPlan {
   int tiles_per_split;  // 64-key tiles per split CTA (0 when n_splits == 1)
   int n_splits;         // 1: the attention kernel writes the output itself
   int persistent;       // unsplit calls of short units: the persistent grid (one CTA per SM walks its units)
+  int decode_rows;      // decode-shaped calls: query rows per unit of the transposed kernel (16 or 32), else 0;
+                        // then n_splits KV ranges of tiles_per_split 128-key tiles, always merged
 };
 
 CtxPlan plan_ctx(int64_t batch, int64_t total_q, int64_t max_pages_per_seq);

@@ -290,22 +290,30 @@ gqa_status nvfp4_paged_ctx_attn(const void* q_fp8, float q_scale, const void* k_
  * range keeps at least 8 tiles.  *persistent = 1 when an unsplit call runs
  * the persistent grid (one CTA per SM walks a share of the units; same
  * result, bit for bit): at least 304 units and max_pages_per_seq <= 48, i.e.
- * short units, whose per-CTA start and end it saves.  Any output pointer may
- * be NULL.
+ * short units, whose per-CTA start and end it saves.  *decode_shaped = 1 when
+ * the call runs the decode-shaped kernel instead (total_q <= batch, i.e. at
+ * most one query per sequence on average, and max_pages_per_seq >= 16): S and
+ * P V computed transposed (keys on the MMA's M dimension, 4 queries x 4 heads
+ * on N), always as KV ranges (*num_splits of *tiles_per_split 128-key tiles)
+ * that the merge combines (*num_launches = 2); its outputs meet the same
+ * parity bar but are not bit-identical to the other kernels'.  Any output
+ * pointer may be NULL.
  */
 gqa_status gqa_ctx_plan(int64_t batch, int64_t total_q, int64_t max_pages_per_seq, int32_t* tiles_per_split,
-                        int32_t* num_splits, int32_t* num_launches, int32_t* persistent);
+                        int32_t* num_splits, int32_t* num_launches, int32_t* persistent, int32_t* decode_shaped);
 
 /*
  * gqa_set_ctx_grid -- test switch: the grid of later unsplit
  * nvfp4_paged_ctx_attn calls (all devices, all threads; process-wide).
  * GQA_CTX_GRID_PLANNED (0) = as gqa_ctx_plan reports; GQA_CTX_GRID_PER_UNIT
  * (1) = one CTA per work unit; GQA_CTX_GRID_PERSISTENT (2) = the persistent
- * grid.  Both grids compute the same result, bit for bit; split-KV calls and
- * the ring-depth study instances (gqa_set_schedule) always run one CTA per
- * unit.  GQA_ERR_INVALID_ARG for another mode (nothing changes).
+ * grid; GQA_CTX_GRID_DECODE_SHAPED (3) = the decode-shaped kernel for every
+ * call.  The first two compute the same result, bit for bit; split-KV calls
+ * and the ring-depth study instances (gqa_set_schedule) always run one CTA
+ * per unit.  Modes 1 and 2 keep calls off the decode-shaped kernel.
+ * GQA_ERR_INVALID_ARG for another mode (nothing changes).
  */
-enum { GQA_CTX_GRID_PLANNED = 0, GQA_CTX_GRID_PER_UNIT = 1, GQA_CTX_GRID_PERSISTENT = 2 };
+enum { GQA_CTX_GRID_PLANNED = 0, GQA_CTX_GRID_PER_UNIT = 1, GQA_CTX_GRID_PERSISTENT = 2, GQA_CTX_GRID_DECODE_SHAPED = 3 };
 gqa_status gqa_set_ctx_grid(int mode);
 
 /*

@@ -216,15 +216,24 @@ def test_decode_plan_covers_capacity():
 
 
 def test_ctx_plan_splits_only_small_calls():
-    """The context attention splits each unit's KV range only when its units
+    """The prefill kernel splits each unit's KV range only when its units
     (8 KV heads x floor((total_q + 63 batch) / 64), a bound on the sequences'
     64-query blocks) leave the 152 SMs idle, into at most 152 / units ranges
-    of at least 8 tiles that cover the table."""
+    of at least 8 tiles that cover the table.  Calls of at most one query per
+    sequence over at least 16 pages take the decode-shaped kernel instead:
+    always ranges of 128-key tiles (at least 4 each, at most 32 ranges) that
+    cover the table, and a merge."""
     for B, tq, mp in [(2, 2, 64), (1, 32, 512), (4, 8192, 32), (2, 8192, 1024), (1, 1, 4), (1, 1, 16),
                       (64, 64, 128), (8, 8, 2048), (1, 500, 100), (3, 5, 5), (1, 64, 16), (9, 9, 4096)]:
         p = gqa.gqa_ctx_plan(B, tq, mp)
         units = 8 * ((tq + 63 * B) // 64)
-        if p["num_splits"] == 1:
+        if p["decode_shaped"]:
+            assert tq <= B and mp >= 16 and p["persistent"] == 0 and p["num_launches"] == 2
+            tiles = (mp + 1) // 2
+            assert 1 <= p["num_splits"] <= 32
+            assert p["num_splits"] * p["tiles_per_split"] >= tiles > (p["num_splits"] - 1) * p["tiles_per_split"]
+            assert p["tiles_per_split"] >= min(4, tiles)
+        elif p["num_splits"] == 1:
             assert p["tiles_per_split"] == 0 and p["num_launches"] == 1
             assert units > 76 or mp < 16
         else:
@@ -233,9 +242,13 @@ def test_ctx_plan_splits_only_small_calls():
             assert p["tiles_per_split"] >= 8
             assert p["num_splits"] * p["tiles_per_split"] >= mp        # the ranges cover every tile
             assert (p["num_splits"] - 1) * p["tiles_per_split"] < mp   # and none lies past the table
-    assert gqa.gqa_ctx_plan(2, 2, 64) == {"tiles_per_split": 8, "num_splits": 8, "num_launches": 2, "persistent": 0}
+    assert gqa.gqa_ctx_plan(2, 2, 64) == {"tiles_per_split": 4, "num_splits": 8, "num_launches": 2, "persistent": 0,
+                                          "decode_shaped": 1}
     assert gqa.gqa_ctx_plan(1, 32, 512) == {"tiles_per_split": 27, "num_splits": 19, "num_launches": 2,
-                                            "persistent": 0}
+                                            "persistent": 0, "decode_shaped": 0}
+    assert gqa.gqa_ctx_plan(64, 64, 128)["decode_shaped"] == 1   # ctx_b64_q1_kv8192
+    assert gqa.gqa_ctx_plan(64, 512, 128)["decode_shaped"] == 0  # ctx_b64_q8_kv8192: 8 queries per sequence
+    assert gqa.gqa_ctx_plan(1, 1, 15)["decode_shaped"] == 0      # short KV
     assert gqa.gqa_ctx_plan(1, 0, 16)["num_launches"] == 0
     with pytest.raises(gqa.GqaError):
         gqa.gqa_ctx_plan(0, 1, 16)
@@ -258,9 +271,9 @@ def test_ctx_plan_takes_persistent_grid_only_for_many_short_units():
 
 
 def test_ctx_grid_switch_validates(L):
-    for mode in (2, 1, 0):
+    for mode in (3, 2, 1, 0):
         assert L.gqa_set_ctx_grid(mode) == OK
-    assert L.gqa_set_ctx_grid(3) == INVALID
+    assert L.gqa_set_ctx_grid(4) == INVALID
     assert L.gqa_set_ctx_grid(-1) == INVALID
     assert b"grid mode" in L.gqa_last_error()
     assert L.gqa_set_ctx_grid(0) == OK

@@ -168,6 +168,23 @@ def test_bounded_waits_expire_in_the_context_kernels():
     assert gqa.gqa_check_device_errors(0) == 0
 
 
+@pytest.fixture
+def prefill_kernel():
+    """Keep calls of at most one query per sequence on the prefill kernel
+    (one CTA per unit, or its split-KV form) instead of the decode-shaped one."""
+    gqa.gqa_set_ctx_grid(gqa.CTX_GRID_PER_UNIT)
+    yield
+    gqa.gqa_set_ctx_grid(gqa.CTX_GRID_PLANNED)
+
+
+@pytest.fixture(params=["planned", "prefill"])
+def grid(request):
+    """Run under the planned kernel choice and under the prefill kernel."""
+    gqa.gqa_set_ctx_grid(gqa.CTX_GRID_PLANNED if request.param == "planned" else gqa.CTX_GRID_PER_UNIT)
+    yield request.param
+    gqa.gqa_set_ctx_grid(gqa.CTX_GRID_PLANNED)
+
+
 def plan_of(x: W.CtxInputs):
     return gqa.gqa_ctx_plan(x.block_table.shape[0], x.q_fp8.shape[0], x.block_table.shape[1])
 
@@ -181,9 +198,9 @@ def plan_of(x: W.CtxInputs):
     ([40], [2000], 1.0),              # M-tile 1 holds queries 32..39 only
     ([33, 64], [1100, 1500], 1.0),    # several units, range boundaries inside the causal diagonal's reach
 ])
-def test_split_kv_shapes(q_lens, kv_lens, out_scale):
+def test_split_kv_shapes(q_lens, kv_lens, out_scale, prefill_kernel):
     x = W.make_ctx_inputs(q_lens, kv_lens, seed=61 + sum(kv_lens), out_scale=out_scale)
-    assert plan_of(x)["num_splits"] > 1
+    assert plan_of(x)["num_splits"] > 1 and plan_of(x)["decode_shaped"] == 0
     check_ctx(run(x), ref(x), f"split q{q_lens} kv{kv_lens}")
 
 
@@ -209,10 +226,15 @@ def test_split_kv_scales_and_host_path():
 
 
 @pytest.mark.parametrize("name", ["ctx_b2_q1_kv4096", "ctx_b1_q32_kv32768"])
-def test_workload_split_rows_full(name):
+def test_workload_split_rows_full(name, grid):
+    """The page rows in full; "2 x 1 x 4096" plans onto the decode-shaped
+    kernel, so it also runs on the prefill kernel's split-KV path."""
     x = W.ctx_workload(name)
-    assert plan_of(x)["num_splits"] > 1
-    check_ctx(run(x), ref(x), name)
+    p = plan_of(x)
+    assert p["num_splits"] > 1
+    if grid == "planned":
+        assert p["decode_shaped"] == (1 if name == "ctx_b2_q1_kv4096" else 0)
+    check_ctx(run(x), ref(x), f"{name} ({grid})")
 
 
 def device_workload(name, **overrides):
@@ -238,12 +260,20 @@ def test_workload_b4_q2048_kv2048_full():
 
 
 @pytest.mark.parametrize("name", ["ctx_b64_q1_kv8192", "ctx_b64_q8_kv8192"])
-def test_decode_shaped_workloads_full(name):
+def test_decode_shaped_workloads_full(name, grid):
     """Decode-shaped NVFP4 calls at a realistic batch (64 sequences of 8192
-    keys, 1 or 8 queries): every row, the benchmark's device-generated inputs."""
+    keys, 1 or 8 queries): every row, the benchmark's device-generated inputs,
+    under the planned kernel (the decode-shaped one for 1 query) and the
+    prefill kernel (512 units fill the GPU: one unsplit launch)."""
+    if grid == "prefill" and name == "ctx_b64_q8_kv8192":
+        pytest.skip("planned onto the prefill kernel already")
     xd, xh = device_workload(name)
-    assert plan_of(xh)["num_splits"] == 1  # 512 units fill the GPU
-    check_ctx(run_dev(xd), ref(xh), name)
+    p = plan_of(xh)
+    if grid == "planned":
+        assert p["decode_shaped"] == (1 if name == "ctx_b64_q1_kv8192" else 0)
+    else:
+        assert p["num_splits"] == 1 and p["decode_shaped"] == 0
+    check_ctx(run_dev(xd), ref(xh), f"{name} ({grid})")
 
 
 def _b2_q4096_kv65536_items():
