@@ -77,7 +77,7 @@ PROFILES = {
     "decode_b8_cap131072": ("decode_split_kernel_decode_b8_cap131072.md", _DEC_SRC),
     "ctx_b4_q2048_kv2048": ("ctx_nvfp4_persistent_kernel_ctx_b4_q2048_kv2048.md", _CTX_SRC),
     "ctx_b2_q4096_kv65536": ("ctx_nvfp4_kernel_ctx_b2_q4096_kv65536.md", _CTX_SRC),
-    "ctx_b64_q1_kv8192": ("ctx_nvfp4_kernel_ctx_b64_q1_kv8192.md", _CTX_SRC),
+    "ctx_b64_q1_kv8192": ("ctx_nvfp4_decode_kernel_ctx_b64_q1_kv8192.md", _CTX_SRC),
 }
 
 
