@@ -25,21 +25,24 @@
 // kN values per key instead of 128.
 //
 // Measured against ctx_nvfp4_kernel on 64 sequences x 1 query x 8192 keys:
-// 1.05x (outputs within the same parity bar).  Both kernels settle near 0.6
-// us per page and SM; the tile rate follows the recycling of the K/V slots
-// (dequantisation -> S^T -> softmax -> O^T -> the slot's next tile): 2 slots
-// 0.76x, 3 slots 1.0x, more do not fit beside the page ring, and a deeper page
-// ring (7 or 12 stages) or non-suspending waits change nothing.
+// 1.06x (outputs within the same parity bar).  K and V tiles recycle through
+// separate rings: a K slot is free once S^T has read it, a V slot once O^T
+// has (three shared K/V slots: 1.05x; two: 0.80x).  Timing probes (invalid
+// output): the page copies alone take 0.63 of the kernel's time (4 page
+// stages, ~37 KB in flight per SM), the work on the pages alone 0.88; a third
+// dequantiser group, a deeper page ring or one O^T product per tile gain
+// little or nothing.
 //
 // Work unit: (sequence b, chunk of kN/4 queries, KV head g, KV range);
 // grid.x = 8 KV heads x a bound on the (sequence, chunk) pairs from
 // host-known sizes (CTAs past the last unit leave at once), grid.y = KV
 // ranges of tiles_per_range 128-key tiles.
-// Warp roles (16 warps): 0 producer of packed pages (one page per stage),
+// Warp roles (16 warps): 0 producer of packed pages (one page per stage, 4 stages),
 // 1 issuer of S^T, 2 issuer of O^T, 3 Q loader, 4-7 softmax (TMEM lane =
 // key of the tile) and epilogue (TMEM lane = head dim), 8-11 and 12-15
 // dequantisers of a tile's first and second page.
-// TMEM: two S^T buffers (kN columns each), then O^T (kN columns).
+// TMEM: two S^T buffers (kN columns each), then O^T (kN columns).  Shared
+// memory: 3 K slots (16 KB), 4 V slots (32 KB), 4 page stages (9 KB).
 // Every wait is bounded (2 s); the teardown drains as in ctx_nvfp4_kernel.
 #pragma once
 #include "ctx_kernel.cuh"
@@ -50,19 +53,20 @@ namespace ctx {
 constexpr int kDecKT = 128;                  // keys per tile: two pages
 constexpr int kDecKTile = kDecKT * kD;       // E4M3 K tile: 16 KB
 constexpr int kDecVHalf = kDecKT * 64 * 2;   // one 64-dim half of the F16 V tile: 16 KB
-constexpr int kDecNP = 6;                    // packed-page stages (pages)
-constexpr int kDecNK = 3;                    // dequantised K/V tile slots (48 KB each; 2 measured 0.76x)
+constexpr int kDecNP = 4;                    // packed-page stages (pages)
+constexpr int kDecNKk = 3;                   // dequantised K tile slots (16 KB each): free once S^T completes
+constexpr int kDecNKv = 4;                   // dequantised V tile slots (32 KB each): free once O^T completes
 
 template <int kN>
 struct DecSmem {
-  uint8_t k[kDecNK][kDecKTile];             // K tiles: 128 keys x 128 B, 128B-swizzled (K-major A of S^T)
-  uint8_t v[kDecNK][2 * kDecVHalf];         // V tiles: [half][128 keys][128 B] F16, 128B-swizzled (MN-major A of O^T)
+  uint8_t k[kDecNKk][kDecKTile];            // K tiles: 128 keys x 128 B, 128B-swizzled (K-major A of S^T)
+  uint8_t v[kDecNKv][2 * kDecVHalf];        // V tiles: [half][128 keys][128 B] F16, 128B-swizzled (MN-major A of O^T)
   uint8_t pk[kDecNP][2][kPackedPage];       // [stage][K=0,V=1][slot*64 + byte]
   uint8_t sf[kDecNP][2][kScalePage];        // [stage][K,V][slot*8 + block]
   uint8_t q[kN * 128];                      // Q rows r = 4*query + head, 128B-swizzled (K-major B of S^T)
   uint8_t p[2][2][kN * 128];                // P^T [buffer][keys 0-63 | 64-127][row][128 B] F16, 128B-swizzled
   uint64_t pk_full[kDecNP], pk_empty[kDecNP];
-  uint64_t kv_ready[kDecNK], kv_free[kDecNK];
+  uint64_t kv_ready[kDecNKv], k_free[kDecNKk], v_free[kDecNKv];  // tile j: K slot j % 3, V slot j % 4
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t q_ready, o_final, drain[2];
   uint2 ktab[256];
@@ -203,10 +207,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.pk_full[i]), 1);
       mbar_init(smem_u32(&sm.pk_empty[i]), 4);
     }
-    for (int i = 0; i < kDecNK; ++i) {
+    for (int i = 0; i < kDecNKv; ++i) {
       mbar_init(smem_u32(&sm.kv_ready[i]), 8);  // both dequantiser groups
-      mbar_init(smem_u32(&sm.kv_free[i]), 2);   // S^T and O^T products
+      mbar_init(smem_u32(&sm.v_free[i]), 1);    // the O^T product
     }
+    for (int i = 0; i < kDecNKk; ++i) mbar_init(smem_u32(&sm.k_free[i]), 1);  // the S^T product
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.s_full[i]), 1);
       mbar_init(smem_u32(&sm.s_free[i]), 4);
@@ -294,17 +299,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
       bool ok = wait_all(&sm.q_ready, 0);
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int slot = j % kDecNK;
-        ok = wait_all(&sm.kv_ready[slot], (j / kDecNK) & 1) &&
+        const int ks = j % kDecNKk;
+        ok = wait_all(&sm.kv_ready[j % kDecNKv], (j / kDecNKv) & 1) &&
              (j < 2 || wait_all(&sm.s_free[j & 1], ((j >> 1) - 1) & 1));
         if (!ok) break;
         tc::fence_after_thread_sync();
-        const uint64_t dk = tc::sw128_desc(smem_u32(sm.k[slot]));
+        const uint64_t dk = tc::sw128_desc(smem_u32(sm.k[ks]));
         if (tc::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) tc::mma_e4m3(tm + (uint32_t)(j & 1) * kN, dk + 2 * kk, dq + 2 * kk, idS, kk > 0);
           tc::commit(smem_u32(&sm.s_full[j & 1]));
-          tc::commit(smem_u32(&sm.kv_free[slot]));
+          tc::commit(smem_u32(&sm.k_free[ks]));
         }
         __syncwarp();
       }
@@ -317,11 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0) + 2 * kN;
       bool ok = true;
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int slot = j % kDecNK;
-        ok = wait_all(&sm.kv_ready[slot], (j / kDecNK) & 1) && wait_all(&sm.p_full[j & 1], (j >> 1) & 1);
+        const int vs = j % kDecNKv;
+        ok = wait_all(&sm.kv_ready[vs], (j / kDecNKv) & 1) && wait_all(&sm.p_full[j & 1], (j >> 1) & 1);
         if (!ok) break;
         tc::fence_after_thread_sync();
-        const uint64_t dv = tc::sw128_desc_lbo(smem_u32(sm.v[slot]), kDecVHalf);
+        const uint64_t dv = tc::sw128_desc_lbo(smem_u32(sm.v[vs]), kDecVHalf);
         const uint64_t dp = tc::sw128_desc(smem_u32(sm.p[j & 1][0]));
         if (tc::elect_one()) {
 #pragma unroll
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_f16(tm, a_d, b_d, idO, (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc::commit(smem_u32(&sm.p_free[j & 1]));
-          tc::commit(smem_u32(&sm.kv_free[slot]));
+          tc::commit(smem_u32(&sm.v_free[vs]));
         }
         __syncwarp();
       }
@@ -516,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pg = 2 * j + grp;  // page of the range
       const bool have = pg < n_pages;
       const int st = pg % kDecNP;
-      const int slot = j % kDecNK;
+      const int ks = j % kDecNKk, vs = j % kDecNKv;
       uint4 packed[2][2];
       uint2 ktab[2][2], vtab[2][2];
       if (have) {
@@ -543,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ktab[it][0] = ktab[it][1] = vtab[it][0] = vtab[it][1] = sm.ktab[0];
         }
       }
-      if (j >= kDecNK && !wait_all(&sm.kv_free[slot], ((j / kDecNK) - 1) & 1)) {
+      if ((j >= kDecNKk && !wait_all(&sm.k_free[ks], ((j / kDecNKk) - 1) & 1)) ||
+          (j >= kDecNKv && !wait_all(&sm.v_free[vs], ((j / kDecNKv) - 1) & 1))) {
         ok = false;
         break;
       }
@@ -553,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int it = 0; it < 2; ++it)
           if (key_begin + j * kDecKT + 64 * grp + key0 + 32 * it >= kv_len) packed[kv][it] = make_uint4(0u, 0u, 0u, 0u);
-      uint8_t* kt = sm.k[slot];
+      uint8_t* kt = sm.k[ks];
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
         const int row = 64 * grp + key0 + 32 * it;
@@ -562,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(kt + swz(row, 2 * pb + 1)) =
             dequant16_e4m3(make_uint2(packed[0][it].z, packed[0][it].w), ktab[it][1]);
       }
-      uint8_t* half = sm.v[slot] + (pb >> 1) * kDecVHalf;
+      uint8_t* half = sm.v[vs] + (pb >> 1) * kDecVHalf;
 #pragma unroll
       for (int it = 0; it < 2; ++it) {
         const int row = 64 * grp + key0 + 32 * it;
@@ -577,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&sm.kv_ready[slot]));
+        mbar_arrive(smem_u32(&sm.kv_ready[vs]));
         if (have) mbar_arrive(smem_u32(&sm.pk_empty[st]));
       }
     }
