@@ -68,16 +68,19 @@ FALLBACK_HBM = 6800.0
 FALLBACK_BF16 = 1900.0
 FP8_OVER_BF16 = 2.0        # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 HBM_NOMINAL_GBS = 7900.0   # GB300 HBM3e, nominal: a read-only stream may exceed the measured copy figure
-# Committed ncu summaries: DRAM bytes per launch, valid while the kernel source digest matches.
+# Committed ncu summaries: DRAM bytes per launch, valid while the digest of the sources the kernel is built
+# from (its header plus the shared ones) matches.
 _DEC_SRC = ["decode.cu", "common.cuh", "kernels.h"]
-_CTX_SRC = ["ctx_kernel.cuh", "ctx_persistent.cuh", "ctx_decode.cuh", "ctx_nvfp4.cu", "common.cuh", "nvfp4.cuh",
-            "tcgen05.cuh", "kernels.h"]
+_CTX_COMMON = ["ctx_kernel.cuh", "ctx_nvfp4.cu", "common.cuh", "nvfp4.cuh", "tcgen05.cuh", "kernels.h"]
+_CTX_SRC = _CTX_COMMON                                  # one CTA per unit (and its split-KV form)
+_CTX_PERSISTENT_SRC = _CTX_COMMON + ["ctx_persistent.cuh"]
+_CTX_DECODE_SRC = _CTX_COMMON + ["ctx_decode.cuh"]
 PROFILES = {
     "decode_b64_cap8192": ("decode_split_kernel_decode_b64_cap8192.md", _DEC_SRC),
     "decode_b8_cap131072": ("decode_split_kernel_decode_b8_cap131072.md", _DEC_SRC),
-    "ctx_b4_q2048_kv2048": ("ctx_nvfp4_persistent_kernel_ctx_b4_q2048_kv2048.md", _CTX_SRC),
+    "ctx_b4_q2048_kv2048": ("ctx_nvfp4_persistent_kernel_ctx_b4_q2048_kv2048.md", _CTX_PERSISTENT_SRC),
     "ctx_b2_q4096_kv65536": ("ctx_nvfp4_kernel_ctx_b2_q4096_kv65536.md", _CTX_SRC),
-    "ctx_b64_q1_kv8192": ("ctx_nvfp4_decode_kernel_ctx_b64_q1_kv8192.md", _CTX_SRC),
+    "ctx_b64_q1_kv8192": ("ctx_nvfp4_decode_kernel_ctx_b64_q1_kv8192.md", _CTX_DECODE_SRC),
 }
 
 
