@@ -35,6 +35,11 @@ constexpr size_t kMaxSmemPerBlock = 232448;
 // Units a CTA's producer may describe ahead of the consumers.
 constexpr int kUnitRing = 8;
 
+// A softmax warp's 32 output rows (8 queries x 4 heads) for one round of 32
+// of the 128 output columns: the box [8 tokens][4 heads][32 d] of the output
+// tensor map, dense.
+constexpr int kOStage = 32 * 32;
+
 // One work unit as the producer describes it to the other roles.
 struct Unit {
   int64_t qo;          // first output row of the sequence
@@ -50,6 +55,7 @@ struct PSmem {
   uint8_t q[kQBuf][2][kQTile];      // [unit % kQBuf][M-tile] Q (128B-swizzled, K-major A operand)
   uint8_t k[kNK][kKVTile];          // E4M3 K tiles (128B-swizzled, K-major B operand of S = Q K^T)
   uint8_t v[kNK][2 * kVHalf];       // V tiles as F16 (128B-swizzled, MN-major B operand of O += P V)
+  uint8_t ostage[8][kOStage];       // [softmax warp] one 32-column round of its output rows, a TMA store's source
   uint8_t pk[kNP][2][kPackedPage];  // [stage][K=0,V=1][slot*64 + byte]
   uint8_t sf[kNP][2][kScalePage];   // [stage][K,V][slot*8 + block]
   uint64_t pk_full[kNP], pk_empty[kNP];
@@ -113,7 +119,8 @@ static __device__ Unit unit_of(const CtxArgs& a, int k) {
 template <int kNP, int kNK>
 __global__ void __launch_bounds__(kThreads, 1)
     ctx_nvfp4_persistent_kernel(const __grid_constant__ CtxArgs a, const __grid_constant__ CUtensorMap q_map,
-                                const float scale_log2, const float inv_out_scale) {
+                                const __grid_constant__ CUtensorMap out_map, const float scale_log2,
+                                const float inv_out_scale) {
   static_assert(kNK >= 2 && kNP >= 2, "rings need at least two slots");
   constexpr int kQBuf = q_buffers<kNP, kNK>();
   using SM = PSmemOf<kNP, kNK>;
@@ -580,6 +587,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float inv = (l > 0.f) ? inv_out_scale / l : 0.f;
       uint8_t* dst = a.out + ((qo + qrow) * kHq + g * kGroup + hh) * kD;
+      // The warp's rows are 8 consecutive queries x the group's 4 heads: lane
+      // L holds query L / 4, head L % 4, i.e. 32 bytes at offset 32 L of the
+      // box [8 tokens][4 heads][32 d] of a round.  When all 32 rows are rows
+      // of this sequence (within [0, total_q)), each round goes through the
+      // warp's staging buffer as one TMA store, which writes whole 512-byte
+      // token spans; otherwise (a sequence's last block, or an invalid
+      // qo_indptr) every row that is stored at all is stored by its thread.
+      const bool tma_rows = __all_sync(0xffffffffu, row_ok);
+      uint8_t* stage = sm.ostage[warp - 4];
+      const int z = (int)(qo + qrow) - (lane >> 2);  // first query of the warp's rows (valid when tma_rows)
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
@@ -598,7 +615,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 y = __fmul2_rn(make_float2(u2f(o[4 * i + 2]), u2f(o[4 * i + 3])), inv2);
           pk[i] = f4_to_e4m3x4(x.x, x.y, y.x, y.y);
         }
-        if (row_ok) {
+        if (tma_rows) {
+          // the previous store from this buffer has read it
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          *reinterpret_cast<uint4*>(stage + 32 * lane) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(stage + 32 * lane + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tma_store_3d(&out_map, 32 * c, g * kGroup, z, smem_u32(stage));
+        } else if (row_ok) {
           *reinterpret_cast<uint4*>(dst + 32 * c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           *reinterpret_cast<uint4*>(dst + 32 * c + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
@@ -606,6 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.unit_empty[us]));
     }
+    // the output stores complete before the CTA ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     if (!ok) failed = true;
   } else {
     // ---------------------------------------------------------- dequantisers
@@ -728,8 +757,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // launched-unit bound (8 KV heads x query blocks); the CTAs find the real
 // units themselves.
 template <int kNP, int kNK>
-static cudaError_t launch_persistent(const CtxArgs& a, const CUtensorMap& q_map, int64_t units, float scale_log2,
-                                     float inv_out_scale, cudaStream_t stream) {
+static cudaError_t launch_persistent(const CtxArgs& a, const CUtensorMap& q_map, const CUtensorMap& out_map,
+                                     int64_t units, float scale_log2, float inv_out_scale, cudaStream_t stream) {
   static std::atomic<uint64_t> ready{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -748,7 +777,8 @@ static cudaError_t launch_persistent(const CtxArgs& a, const CUtensorMap& q_map,
   if (e != cudaSuccess) return e;
   if (units < 1 || sms < 1) return cudaErrorInvalidConfiguration;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
-  ctx_nvfp4_persistent_kernel<kNP, kNK><<<grid, kThreads, smem, stream>>>(a, q_map, scale_log2, inv_out_scale);
+  ctx_nvfp4_persistent_kernel<kNP, kNK><<<grid, kThreads, smem, stream>>>(a, q_map, out_map, scale_log2,
+                                                                           inv_out_scale);
   return cudaGetLastError();
 }
 
