@@ -168,10 +168,10 @@ cudaError_t make_q_map(const uint8_t* q, int64_t total_q, CUtensorMap* map) {
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, map);
 }
 
-// Tensor map over the output: boxes of [8 tokens][4 heads][32 d] (one
-// softmax warp's rows, one round of 32 columns), dense, for TMA stores.
+// Tensor map over the output: boxes of [8 tokens][4 heads][128 d] (one
+// softmax warp's rows), 128-byte swizzle, for TMA stores.
 cudaError_t make_out_map(uint8_t* out, int64_t total_q, CUtensorMap* map) {
-  return make_qo_map(out, total_q, 32u, 8u, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, map);
+  return make_qo_map(out, total_q, (uint32_t)kD, 8u, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, map);
 }
 
 // The merge of the split partials, launched as a programmatic dependent grid:

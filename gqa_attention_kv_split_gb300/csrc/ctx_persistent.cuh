@@ -35,10 +35,10 @@ constexpr size_t kMaxSmemPerBlock = 232448;
 // Units a CTA's producer may describe ahead of the consumers.
 constexpr int kUnitRing = 8;
 
-// A softmax warp's 32 output rows (8 queries x 4 heads) for one round of 32
-// of the 128 output columns: the box [8 tokens][4 heads][32 d] of the output
-// tensor map, dense.
-constexpr int kOStage = 32 * 32;
+// A softmax warp's 32 output rows (8 queries x 4 heads, 128 bytes each): the
+// box [8 tokens][4 heads][128 d] of the output tensor map, staged for its TMA
+// store in the warp's quarter of the unit's Q buffer (of its M-tile).
+constexpr int kOStage = 32 * kD;
 
 // One work unit as the producer describes it to the other roles.
 struct Unit {
@@ -55,7 +55,6 @@ struct PSmem {
   uint8_t q[kQBuf][2][kQTile];      // [unit % kQBuf][M-tile] Q (128B-swizzled, K-major A operand)
   uint8_t k[kNK][kKVTile];          // E4M3 K tiles (128B-swizzled, K-major B operand of S = Q K^T)
   uint8_t v[kNK][2 * kVHalf];       // V tiles as F16 (128B-swizzled, MN-major B operand of O += P V)
-  uint8_t ostage[8][kOStage];       // [softmax warp] one 32-column round of its output rows, a TMA store's source
   uint8_t pk[kNP][2][kPackedPage];  // [stage][K=0,V=1][slot*64 + byte]
   uint8_t sf[kNP][2][kScalePage];   // [stage][K,V][slot*8 + block]
   uint64_t pk_full[kNP], pk_empty[kNP];
@@ -63,7 +62,7 @@ struct PSmem {
   uint64_t s_full[2][2];                  // [M-tile][buffer]: S computed
   uint64_t p_full[2][2], p_free[2][2];    // [M-tile][buffer]: P written / the P V that read it completed
   uint64_t o_final[2];                    // [M-tile]: every MMA of the unit's M-tile complete
-  uint64_t q_ready[kQBuf], q_free[kQBuf];  // Q of a buffer loaded / read by the unit's last S
+  uint64_t q_ready[kQBuf], q_free[kQBuf];  // Q of a buffer loaded / free (the unit's staged output stored)
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];  // descriptor written / read by all 15 consumer warps
   uint64_t drain[3];                // teardown after an expired wait: MMAs of issuer warps 1..3 complete
   Unit unit[kUnitRing];
@@ -171,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kQBuf; ++i) {
       mbar_init(smem_u32(&sm.q_ready[i]), 1);
-      mbar_init(smem_u32(&sm.q_free[i]), 2);  // the last S of each M-tile
+      mbar_init(smem_u32(&sm.q_free[i]), 8);  // the softmax warps of both M-tiles, after their epilogue
     }
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(smem_u32(&sm.unit_full[i]), 1);
@@ -302,10 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // queued behind a P V the softmax is not waiting for.  The whole warp
     // runs this code (descriptor arithmetic stays warp-uniform, which keeps
     // it in the uniform datapath the MMA reads); one elected lane issues each
-    // MMA and commit.  After a unit's last S the commit on q_free releases
-    // its Q buffer.  M-tile 1 holds queries q0 + 32 .. q0 + 63; when none of
-    // them exists (a sequence's last block of at most 32 queries) it is not
-    // computed: its issuer only releases the K/V slots and the Q buffer.
+    // MMA and commit.  (The unit's Q buffer is released by the softmax warps,
+    // which stage the unit's output there.)  M-tile 1 holds queries q0 + 32
+    // .. q0 + 63; when none of them exists (a sequence's last block of at most
+    // 32 queries) it is not computed: its issuer only releases the K/V slots.
     const int T = warp == 1 ? 0 : 1;
     constexpr uint32_t idS = tc::idesc_e4m3_f32(128, kKT, false);  // B = K tile, K-major
     const uint64_t dk0 = tc::sw128_desc(smem_u32(sm.k[0]));
@@ -326,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_all(&sm.kv_ready[gt % kNK], (gt / kNK) & 1);
           if (ok && lane == 0) mbar_arrive(smem_u32(&sm.kv_free[gt % kNK]));
         }
-        if (ok && lane == 0) mbar_arrive(smem_u32(&sm.q_free[qbuf]));
       } else {
         const uint64_t dq = tc::sw128_desc(smem_u32(sm.q[qbuf][T]));
         for (int j = 0; j < w.n_tiles; ++j, ++gt, ++sc) {
@@ -344,8 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        if (ok && tc::elect_one()) tc::commit(smem_u32(&sm.q_free[qbuf]));
-        __syncwarp();
       }
     }
     if (!ok) failed = true;
@@ -412,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tT = tmem + lane_off + (uint32_t)T * kTmemPerTile;
     const uint32_t tO = tT + kTmemO;
     const bool neg_scale = scale_log2 < 0.f;
-    int sc = 0, oc = 0;  // S tiles of this M-tile, units whose O_T was completed
+    int sc = 0, oc = 0, qk = 0;  // S tiles of this M-tile, units whose O_T was completed, units with tiles
     bool ok = true;
     for (int k = 0; ok; ++k) {
       // Only what the tile loop needs is read here; the epilogue reads the
@@ -587,47 +583,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float inv = (l > 0.f) ? inv_out_scale / l : 0.f;
       uint8_t* dst = a.out + ((qo + qrow) * kHq + g * kGroup + hh) * kD;
-      // The warp's rows are 8 consecutive queries x the group's 4 heads: lane
-      // L holds query L / 4, head L % 4, i.e. 32 bytes at offset 32 L of the
-      // box [8 tokens][4 heads][32 d] of a round.  When all 32 rows are rows
-      // of this sequence (within [0, total_q)), each round goes through the
-      // warp's staging buffer as one TMA store, which writes whole 512-byte
-      // token spans; otherwise (a sequence's last block, or an invalid
-      // qo_indptr) every row that is stored at all is stored by its thread.
-      const bool tma_rows = __all_sync(0xffffffffu, row_ok);
-      uint8_t* stage = sm.ostage[warp - 4];
+      // The warp's rows are 8 consecutive queries x the group's 4 heads (lane
+      // L: query L / 4, head L % 4), i.e. the box [8 tokens][4 heads][128 d]
+      // of the output tensor map.  When all 32 are rows of this sequence within
+      // [0, total_q) and the unit had tiles, they are staged in the unit's Q
+      // buffer -- every S product that read it has completed (o_final, or no
+      // product of this M-tile) -- at the 128-byte-swizzled place the tensor map
+      // reads (row L, 16-byte chunk i at chunk i ^ (L % 8)) and written by one
+      // TMA store; otherwise every row that is stored at all is stored by its
+      // thread.  The Q buffer goes back to the producer (q_free) once the
+      // stores have read it: eight arrivals, one per warp of each computed
+      // M-tile -- M-tile 0's warps arrive twice when M-tile 1 was not
+      // computed, since M-tile 1's warps then wait for nothing and could
+      // otherwise arrive for a later unit's use of the buffer first.
+      const bool q_held = *reinterpret_cast<const volatile int*>(&wd.n_tiles) > 0;
+      const int qbuf = qk % kQBuf;
+      const bool tma_rows = __all_sync(0xffffffffu, row_ok) && q_held;
+      uint8_t* stage = sm.q[qbuf][T] + kOStage * sub;
       const int z = (int)(qo + qrow) - (lane >> 2);  // first query of the warp's rows (valid when tma_rows)
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
+      for (int h = 0; h < 2; ++h) {  // 64 columns at a time: two TMEM loads in flight
+        uint32_t o0[32], o1[32];
         if (have_o) {
-          tc::ld32(tO + 32 * c, o);
+          tc::ld32(tO + 64 * h, o0);
+          tc::ld32(tO + 64 * h + 32, o1);
           tc::ld_wait();
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
+          for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0u;
         }
-        uint32_t pk[8];
+        uint32_t pk[16];
         const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float2 x = __fmul2_rn(make_float2(u2f(o[4 * i]), u2f(o[4 * i + 1])), inv2);
-          const float2 y = __fmul2_rn(make_float2(u2f(o[4 * i + 2]), u2f(o[4 * i + 3])), inv2);
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t* o = i < 8 ? o0 : o1;
+          const int b = 4 * (i & 7);
+          const float2 x = __fmul2_rn(make_float2(u2f(o[b]), u2f(o[b + 1])), inv2);
+          const float2 y = __fmul2_rn(make_float2(u2f(o[b + 2]), u2f(o[b + 3])), inv2);
           pk[i] = f4_to_e4m3x4(x.x, x.y, y.x, y.y);
         }
         if (tma_rows) {
-          // the previous store from this buffer has read it
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
-          *reinterpret_cast<uint4*>(stage + 32 * lane) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(stage + 32 * lane + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tma_store_3d(&out_map, 32 * c, g * kGroup, z, smem_u32(stage));
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(stage + 128 * lane + 16 * ((4 * h + i) ^ (lane & 7))) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         } else if (row_ok) {
-          *reinterpret_cast<uint4*>(dst + 32 * c) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(dst + 32 * c + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(dst + 64 * h + 16 * i) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
+      }
+      if (tma_rows) {
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tma_store_3d(&out_map, 0, g * kGroup, z, smem_u32(stage));
+      }
+      if (q_held) {
+        if (lane == 0 && (T == 0 || n_mine > 0)) {
+          if (tma_rows) bulk_wait_read_all();
+          mbar_arrive_n(smem_u32(&sm.q_free[qbuf]), (T == 0 && !(wd.q0 + kQT < q_len)) ? 2u : 1u);
+        }
+        ++qk;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.unit_empty[us]));
