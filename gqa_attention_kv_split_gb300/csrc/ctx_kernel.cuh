@@ -231,26 +231,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// 3-D tiled TMA store shared -> global as one bulk async-group of the issuing
-// thread.  The shared source must have been written and made visible to the
-// async proxy (fence_proxy_async_smem) before the call.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n\t"
-      "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(x), "r"(y), "r"(z), "r"(src)
-      : "memory");
-}
-
-// The issuing thread's bulk stores have read their shared sources (the
-// buffers may be written again).
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// The issuing thread's bulk stores are complete (their writes performed).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 template <bool kSplit, int kNP, int kNK>
 __global__ void __launch_bounds__(kThreads, 1)
     ctx_nvfp4_kernel(const __grid_constant__ CtxArgs a, const __grid_constant__ CUtensorMap q_map, const float scale_log2,

@@ -138,10 +138,9 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 std::once_flag g_encode_once;
 EncodeTiledFn g_encode = nullptr;
 
-// A tensor map over a [total_q][32 heads][128 d] byte tensor (q or the
-// output) with boxes of [box_tokens][4 heads][box_d].
-cudaError_t make_qo_map(const uint8_t* t, int64_t total_q, uint32_t box_d, uint32_t box_tokens,
-                        CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promotion, CUtensorMap* map) {
+// Tensor map over q [total_q][32 heads][128 d] (E4M3 bytes): boxes of
+// [32 tokens][4 heads][128 d], 128-byte swizzle, zero fill out of range.
+cudaError_t make_q_map(const uint8_t* q, int64_t total_q, CUtensorMap* map) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult qr;
@@ -153,25 +152,12 @@ cudaError_t make_qo_map(const uint8_t* t, int64_t total_q, uint32_t box_d, uint3
   if (!g_encode) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kHq, (cuuint64_t)total_q};
   const cuuint64_t strides[2] = {(cuuint64_t)kD, (cuuint64_t)kHq * kD};
-  const cuuint32_t box[3] = {box_d, (cuuint32_t)kGroup, box_tokens};
+  const cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)kGroup, (cuuint32_t)kQT};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(t), dims, strides, box,
-                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promotion,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(q), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-// Tensor map over q: boxes of [32 tokens][4 heads][128 d] (one M-tile),
-// 128-byte swizzle, zero fill out of range.
-cudaError_t make_q_map(const uint8_t* q, int64_t total_q, CUtensorMap* map) {
-  return make_qo_map(q, total_q, (uint32_t)kD, (uint32_t)kQT, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, map);
-}
-
-// Tensor map over the output: boxes of [8 tokens][4 heads][128 d] (one
-// softmax warp's rows), 128-byte swizzle, for TMA stores.
-cudaError_t make_out_map(uint8_t* out, int64_t total_q, CUtensorMap* map) {
-  return make_qo_map(out, total_q, (uint32_t)kD, 8u, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, map);
 }
 
 // The merge of the split partials, launched as a programmatic dependent grid:
@@ -290,13 +276,9 @@ cudaError_t launch_ctx(const CtxArgs& a, const CtxPlan& plan, void* workspace, c
       return launch_ctx_study(a, q_map, (unsigned)grid, scale_log2, inv_out_scale, st ? st : kCtxStagesDefault,
                               sl ? sl : kCtxSlotsDefault, stream);
     const int mode = schedule_ctx_grid();
-    if (mode == 2 || (mode == 0 && plan.persistent)) {
-      alignas(64) CUtensorMap out_map;
-      e = make_out_map(a.out, a.total_q, &out_map);
-      if (e != cudaSuccess) return e;
-      return launch_persistent<kCtxStagesPersistent, kCtxSlotsDefault>(a, q_map, out_map, grid, scale_log2,
-                                                                          inv_out_scale, stream);
-    }
+    if (mode == 2 || (mode == 0 && plan.persistent))
+      return launch_persistent<kCtxStagesPersistent, kCtxSlotsDefault>(a, q_map, grid, scale_log2, inv_out_scale,
+                                                                          stream);
     return launch_attention<false, kCtxStagesDefault, kCtxSlotsDefault>(
         a, q_map, dim3((unsigned)grid, 1), scale_log2, inv_out_scale, 0, nullptr, nullptr, stream);
   }

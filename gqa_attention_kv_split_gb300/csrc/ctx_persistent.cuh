@@ -21,6 +21,10 @@
 //    made while the current unit's last tiles and output are finished.
 //  * A unit's first P V overwrites O_T: the softmax warps read the previous
 //    unit's O_T (their epilogue) before they write the P it waits for.
+//  * The epilogue stages each softmax warp's 32 output rows in the finished
+//    unit's Q buffer and stores them query by query (512 contiguous bytes per
+//    instruction instead of 32 partial lines); the softmax warps, not the S
+//    issuers, then release the buffer to the producer.
 // The same loop structure run over one long unit computes a tile ~8 % slower
 // than ctx_nvfp4_kernel (measured on GB300, outputs byte-identical), so the
 // launch plan takes this kernel only for calls of short units (see plan_ctx).
@@ -35,9 +39,8 @@ constexpr size_t kMaxSmemPerBlock = 232448;
 // Units a CTA's producer may describe ahead of the consumers.
 constexpr int kUnitRing = 8;
 
-// A softmax warp's 32 output rows (8 queries x 4 heads, 128 bytes each): the
-// box [8 tokens][4 heads][128 d] of the output tensor map, staged for its TMA
-// store in the warp's quarter of the unit's Q buffer (of its M-tile).
+// A softmax warp's 32 output rows (8 queries x 4 heads, 128 bytes each),
+// staged in the warp's quarter of the unit's Q buffer (of its M-tile).
 constexpr int kOStage = 32 * kD;
 
 // One work unit as the producer describes it to the other roles.
@@ -62,7 +65,7 @@ struct PSmem {
   uint64_t s_full[2][2];                  // [M-tile][buffer]: S computed
   uint64_t p_full[2][2], p_free[2][2];    // [M-tile][buffer]: P written / the P V that read it completed
   uint64_t o_final[2];                    // [M-tile]: every MMA of the unit's M-tile complete
-  uint64_t q_ready[kQBuf], q_free[kQBuf];  // Q of a buffer loaded / free (the unit's staged output stored)
+  uint64_t q_ready[kQBuf], q_free[kQBuf];  // Q of a buffer loaded / free (the unit's output, staged there, stored)
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];  // descriptor written / read by all 15 consumer warps
   uint64_t drain[3];                // teardown after an expired wait: MMAs of issuer warps 1..3 complete
   Unit unit[kUnitRing];
@@ -118,8 +121,7 @@ static __device__ Unit unit_of(const CtxArgs& a, int k) {
 template <int kNP, int kNK>
 __global__ void __launch_bounds__(kThreads, 1)
     ctx_nvfp4_persistent_kernel(const __grid_constant__ CtxArgs a, const __grid_constant__ CUtensorMap q_map,
-                                const __grid_constant__ CUtensorMap out_map, const float scale_log2,
-                                const float inv_out_scale) {
+                                const float scale_log2, const float inv_out_scale) {
   static_assert(kNK >= 2 && kNP >= 2, "rings need at least two slots");
   constexpr int kQBuf = q_buffers<kNP, kNK>();
   using SM = PSmemOf<kNP, kNK>;
@@ -584,23 +586,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = (l > 0.f) ? inv_out_scale / l : 0.f;
       uint8_t* dst = a.out + ((qo + qrow) * kHq + g * kGroup + hh) * kD;
       // The warp's rows are 8 consecutive queries x the group's 4 heads (lane
-      // L: query L / 4, head L % 4), i.e. the box [8 tokens][4 heads][128 d]
-      // of the output tensor map.  When all 32 are rows of this sequence within
+      // L: query L / 4, head L % 4), i.e. eight 512-byte spans of the output,
+      // one per query.  When all 32 are rows of this sequence within
       // [0, total_q) and the unit had tiles, they are staged in the unit's Q
       // buffer -- every S product that read it has completed (o_final, or no
-      // product of this M-tile) -- at the 128-byte-swizzled place the tensor map
-      // reads (row L, 16-byte chunk i at chunk i ^ (L % 8)) and written by one
-      // TMA store; otherwise every row that is stored at all is stored by its
-      // thread.  The Q buffer goes back to the producer (q_free) once the
-      // stores have read it: eight arrivals, one per warp of each computed
+      // product of this M-tile) -- row L at 128 L, 16-byte chunk i at chunk
+      // i ^ (L % 8) (no bank conflicts either way), then read back so that
+      // each store instruction writes one query's 512 bytes; otherwise every
+      // row that is stored at all is stored by its thread (32 partial lines
+      // per instruction).  The Q buffer goes back to the producer (q_free)
+      // after the read-back: eight arrivals, one per warp of each computed
       // M-tile -- M-tile 0's warps arrive twice when M-tile 1 was not
       // computed, since M-tile 1's warps then wait for nothing and could
       // otherwise arrive for a later unit's use of the buffer first.
       const bool q_held = *reinterpret_cast<const volatile int*>(&wd.n_tiles) > 0;
       const int qbuf = qk % kQBuf;
-      const bool tma_rows = __all_sync(0xffffffffu, row_ok) && q_held;
+      const bool staged = __all_sync(0xffffffffu, row_ok) && q_held;
       uint8_t* stage = sm.q[qbuf][T] + kOStage * sub;
-      const int z = (int)(qo + qrow) - (lane >> 2);  // first query of the warp's rows (valid when tma_rows)
+      const int z = (int)(qo + qrow) - (lane >> 2);  // first query of the warp's rows (valid when staged)
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {  // 64 columns at a time: two TMEM loads in flight
         uint32_t o0[32], o1[32];
@@ -622,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 y = __fmul2_rn(make_float2(u2f(o[b + 2]), u2f(o[b + 3])), inv2);
           pk[i] = f4_to_e4m3x4(x.x, x.y, y.x, y.y);
         }
-        if (tma_rows) {
+        if (staged) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             *reinterpret_cast<uint4*>(stage + 128 * lane + 16 * ((4 * h + i) ^ (lane & 7))) =
@@ -634,24 +637,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
-      if (tma_rows) {
-        tc::fence_proxy_async_smem();
+      if (staged) {
+        // read back query by query (lane L: head L / 8, 16-byte chunk L % 8)
+        // and store each query's 512 contiguous bytes with one instruction
         __syncwarp();
-        if (lane == 0) tma_store_3d(&out_map, 0, g * kGroup, z, smem_u32(stage));
+        const int hr = lane >> 3, ch = lane & 7;
+        uint8_t* gb = a.out + ((int64_t)z * kHq + g * kGroup + hr) * kD + 16 * ch;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = 4 * i + hr;
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + 128 * row + 16 * (ch ^ (row & 7)));
+          *reinterpret_cast<uint4*>(gb + (int64_t)i * kHq * kD) = v;
+        }
       }
       if (q_held) {
-        if (lane == 0 && (T == 0 || n_mine > 0)) {
-          if (tma_rows) bulk_wait_read_all();
+        __syncwarp();
+        if (lane == 0 && (T == 0 || n_mine > 0))
           mbar_arrive_n(smem_u32(&sm.q_free[qbuf]), (T == 0 && !(wd.q0 + kQT < q_len)) ? 2u : 1u);
-        }
         ++qk;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.unit_empty[us]));
     }
-    // the output stores complete before the CTA ends
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
     if (!ok) failed = true;
   } else {
     // ---------------------------------------------------------- dequantisers
@@ -774,8 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // launched-unit bound (8 KV heads x query blocks); the CTAs find the real
 // units themselves.
 template <int kNP, int kNK>
-static cudaError_t launch_persistent(const CtxArgs& a, const CUtensorMap& q_map, const CUtensorMap& out_map,
-                                     int64_t units, float scale_log2, float inv_out_scale, cudaStream_t stream) {
+static cudaError_t launch_persistent(const CtxArgs& a, const CUtensorMap& q_map, int64_t units, float scale_log2,
+                                     float inv_out_scale, cudaStream_t stream) {
   static std::atomic<uint64_t> ready{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -794,8 +801,7 @@ static cudaError_t launch_persistent(const CtxArgs& a, const CUtensorMap& q_map,
   if (e != cudaSuccess) return e;
   if (units < 1 || sms < 1) return cudaErrorInvalidConfiguration;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
-  ctx_nvfp4_persistent_kernel<kNP, kNK><<<grid, kThreads, smem, stream>>>(a, q_map, out_map, scale_log2,
-                                                                           inv_out_scale);
+  ctx_nvfp4_persistent_kernel<kNP, kNK><<<grid, kThreads, smem, stream>>>(a, q_map, scale_log2, inv_out_scale);
   return cudaGetLastError();
 }
 
