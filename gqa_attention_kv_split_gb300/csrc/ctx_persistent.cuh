@@ -39,6 +39,11 @@ constexpr size_t kMaxSmemPerBlock = 232448;
 // Units a CTA's producer may describe ahead of the consumers.
 constexpr int kUnitRing = 8;
 
+// Arrive `count` times at once on an mbarrier.
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
 // A softmax warp's 32 output rows (8 queries x 4 heads, 128 bytes each),
 // staged in the warp's quarter of the unit's Q buffer (of its M-tile).
 constexpr int kOStage = 32 * kD;
