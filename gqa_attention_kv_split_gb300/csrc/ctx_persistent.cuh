@@ -609,38 +609,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool staged = __all_sync(0xffffffffu, row_ok) && q_held;
       uint8_t* stage = sm.q[qbuf][T] + kOStage * sub;
       const int z = (int)(qo + qrow) - (lane >> 2);  // first query of the warp's rows (valid when staged)
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {  // 64 columns at a time: two TMEM loads in flight
-        uint32_t o0[32], o1[32];
-        if (have_o) {
-          tc::ld32(tO + 64 * h, o0);
-          tc::ld32(tO + 64 * h + 32, o1);
-          tc::ld_wait();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0u;
-        }
-        uint32_t pk[16];
+      // Four rounds of 32 columns; round c + 1's TMEM load is in flight while
+      // round c is converted and staged.
+      auto emit = [&](const uint32_t (&o)[32], int c) {
+        uint32_t pk[8];
         const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t* o = i < 8 ? o0 : o1;
-          const int b = 4 * (i & 7);
-          const float2 x = __fmul2_rn(make_float2(u2f(o[b]), u2f(o[b + 1])), inv2);
-          const float2 y = __fmul2_rn(make_float2(u2f(o[b + 2]), u2f(o[b + 3])), inv2);
+        for (int i = 0; i < 8; ++i) {
+          const float2 x = __fmul2_rn(make_float2(u2f(o[4 * i]), u2f(o[4 * i + 1])), inv2);
+          const float2 y = __fmul2_rn(make_float2(u2f(o[4 * i + 2]), u2f(o[4 * i + 3])), inv2);
           pk[i] = f4_to_e4m3x4(x.x, x.y, y.x, y.y);
         }
         if (staged) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(stage + 128 * lane + 16 * ((4 * h + i) ^ (lane & 7))) =
+          for (int i = 0; i < 2; ++i)
+            *reinterpret_cast<uint4*>(stage + 128 * lane + 16 * ((2 * c + i) ^ (lane & 7))) =
                 make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         } else if (row_ok) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(dst + 64 * h + 16 * i) =
+          for (int i = 0; i < 2; ++i)
+            *reinterpret_cast<uint4*>(dst + 32 * c + 16 * i) =
                 make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
+      };
+      uint32_t oa[32], ob[32];
+      if (have_o) {
+        tc::ld32(tO, oa);
+        tc::ld_wait();
+        tc::ld32(tO + 32, ob);
+        emit(oa, 0);
+        tc::ld_wait();
+        tc::ld32(tO + 64, oa);
+        emit(ob, 1);
+        tc::ld_wait();
+        tc::ld32(tO + 96, ob);
+        emit(oa, 2);
+        tc::ld_wait();
+        emit(ob, 3);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) oa[i] = 0u;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) emit(oa, c);
       }
       if (staged) {
         // read back query by query (lane L: head L / 8, 16-byte chunk L % 8)
